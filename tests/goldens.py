@@ -1,0 +1,79 @@
+"""Loader for the hand-derived golden streams under tests/golden/."""
+from __future__ import annotations
+
+import glob
+import os
+import struct
+
+import numpy as np
+
+GOLDEN_DIR = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden")
+
+
+def distinct_u32(n: int) -> np.ndarray:
+    # (i + 1) * odd constant mod 2^32 is a bijection, so the words are distinct
+    i = np.arange(1, n + 1, dtype=np.uint64)
+    return ((i * np.uint64(2654435761)) & np.uint64(0xFFFFFFFF)).astype(np.uint32)
+
+
+def _make_input(spec: str) -> np.ndarray:
+    kind, *args = spec.split()
+    if kind == "repeat_u32":
+        return np.full(int(args[1]), int(args[0], 0), np.uint32).view(np.uint8)
+    if kind == "bytes":
+        return np.frombuffer(bytes.fromhex(args[0]), np.uint8).copy()
+    if kind == "zero_then_distinct_u32":
+        n = int(args[0])
+        return np.concatenate([np.zeros(n, np.uint32), distinct_u32(n)]).view(np.uint8)
+    raise ValueError(spec)
+
+
+def _layout_stream(layout: str, x: np.ndarray, ws: int, cs: int) -> np.ndarray:
+    out = bytearray()
+    n_chunks = (x.size + cs - 1) // cs
+    for part in layout.split("|"):
+        kind, *args = part.split()
+        if kind == "header":
+            out += struct.pack("<IHBBIIQQ", 0x5A4C5047, 1, ws, 0, cs, n_chunks, x.size,
+                               int(args[0], 0))
+        elif kind == "entry":
+            out += struct.pack("<II", int(args[0], 0), int(args[1], 0))
+        elif kind == "raw_copy_of_input":
+            out += bytes(x[int(args[0]):int(args[1])])
+        else:
+            raise ValueError(part)
+    return np.frombuffer(bytes(out), np.uint8).copy()
+
+
+def load_all():
+    cases = []
+    for path in sorted(glob.glob(os.path.join(GOLDEN_DIR, "*.txt"))):
+        meta = {}
+        hexlines = []
+        in_stream = False
+        with open(path) as f:
+            for line in f:
+                line = line.strip()
+                if not line or line.startswith("#"):
+                    continue
+                if in_stream:
+                    hexlines.append(line.replace(" ", ""))
+                    continue
+                key, _, val = line.partition(":")
+                val = val.strip()
+                if key == "stream":
+                    in_stream = True
+                    continue
+                meta[key] = val
+        ws = int(meta["word_size"])
+        cs = int(meta["chunk_size"])
+        levels = [int(v) for v in meta["match_level"].split()]
+        x = _make_input(meta["input"])
+        assert x.size == int(meta["n_bytes"])
+        if hexlines:
+            stream = np.frombuffer(bytes.fromhex("".join(hexlines)), np.uint8).copy()
+        else:
+            stream = _layout_stream(meta["stream_layout"], x, ws, cs)
+        cases.append(dict(name=os.path.basename(path), ws=ws, cs=cs, levels=levels, x=x,
+                          stream=stream))
+    return cases

@@ -1,0 +1,301 @@
+"""Pins of the CPU oracle against facts fixed outside itself.
+
+Each check is chosen so that a plausible slip in the oracle (a wrong window
+bound, a dropped AND, a farthest-instead-of-nearest offset, a table that
+admits the current sub-block, min instead of max in a bucket, an off-by-one
+cap, a flipped flag polarity, a wrong raw threshold) fails at least one:
+
+* brute-force longest match on tiny inputs (exhaustive over a 2-symbol
+  alphabet, random over small alphabets);
+* closed forms: constant chunk, period-p chunk (p <= 32) at level 0, period-40
+  chunk at level 1 (only the hashed table can see it, and only from earlier
+  sub-blocks, keeping the most recent position), zero chunk, incompressible
+  chunk;
+* hand-derived golden streams (tests/golden/);
+* structural invariants and an independent replay decoder on every stream;
+* round trip through the oracle's own decoder, both levels, all geometries.
+"""
+import itertools
+
+import numpy as np
+import pytest
+
+import goldens
+import streamcheck
+
+
+# ----------------------------------------------------------------------------
+# brute force longest match over the near window
+# ----------------------------------------------------------------------------
+def brute_near(w):
+    """Direct definition: for each i, the longest run w[i+k] == w[i+k-o] over
+    1 <= o <= min(32, i), capped at min(255, E - i); the smallest o wins ties."""
+    E = len(w)
+    L = np.zeros(E, np.uint8)
+    O = np.zeros(E, np.uint8)
+    for i in range(E):
+        cap = min(255, E - i)
+        best, bo = 0, 0
+        for o in range(1, min(32, i) + 1):
+            k = 0
+            while k < cap and w[i + k] == w[i + k - o]:
+                k += 1
+            if k > best:
+                best, bo = k, o
+        L[i], O[i] = best, bo
+    return L, O
+
+
+def test_near_exhaustive_binary_len10(orc):
+    for bits in itertools.product((0, 1), repeat=10):
+        w = np.array(bits, np.uint32) + 7
+        L, O = orc.near_matches(w)
+        bl, bo = brute_near(list(w))
+        assert np.array_equal(L, bl) and np.array_equal(O, bo), bits
+
+
+@pytest.mark.parametrize("alphabet,E", [(2, 40), (3, 64), (4, 64), (3, 300), (40, 96)])
+def test_near_random_small_alphabet(orc, alphabet, E):
+    rng = np.random.default_rng(1000 + alphabet * 7 + E)
+    for _ in range(20):
+        w = rng.integers(0, alphabet, E).astype(np.uint32) * 0x01010101
+        L, O = orc.near_matches(w)
+        bl, bo = brute_near(list(w))
+        assert np.array_equal(L, bl)
+        assert np.array_equal(O, bo)
+
+
+def test_near_window_is_32(orc):
+    # period 32 is seen, period 33 is not
+    base = goldens.distinct_u32(33)
+    for p, expect in ((32, True), (33, False)):
+        w = np.tile(base[:p], 600 // p + 1)[:600]
+        L, _ = orc.near_matches(w)
+        assert bool(L[p:].any()) is expect
+        assert not L[:p].any()
+
+
+def test_near_length_cap_and_chunk_end(orc):
+    w = np.full(512, 5, np.uint32)
+    L, O = orc.near_matches(w)
+    assert L[0] == 0 and L[1] == 255 and O[1] == 1
+    assert L[256] == 255 and L[300] == 212 and L[511] == 1
+    assert (O[1:] == 1).all()
+
+
+# ----------------------------------------------------------------------------
+# closed forms through the whole-chunk encoder
+# ----------------------------------------------------------------------------
+def test_constant_chunk_both_levels(orc):
+    x = np.full(512, 0x01020304, np.uint32).view(np.uint8)
+    for lvl in (0, 1):
+        blk, items, dbytes = orc.encode_chunk(x, 4, 2048, lvl)
+        assert (items, dbytes) == (4, 10)
+        assert blk.size == 16
+        flags = blk[:4].view(np.uint32)[0]
+        assert flags == 0b1110
+        assert list(blk[4:16]) == [4, 3, 2, 1, 255, 1, 255, 1, 1, 1, 0, 0]
+
+
+@pytest.mark.parametrize("p", [1, 2, 7, 16, 31, 32])
+def test_period_p_level0_closed_form(orc, p):
+    E = 512
+    w = np.tile(goldens.distinct_u32(p), E // p + 1)[:E]
+    blk, items, dbytes = orc.encode_chunk(w.view(np.uint8), 4, 2048, 0)
+    n_match = -(-(E - p) // 255)
+    assert items == p + n_match
+    assert dbytes == 4 * p + 2 * n_match
+    parsed = streamcheck.parse(_one_chunk_stream(orc, w.view(np.uint8), 4, 2048, 0))
+    toks = parsed["chunks"][0]["items"]
+    assert [t[0] for t in toks] == ["L"] * p + ["M"] * n_match
+    lens = [t[1] for t in toks[p:]]
+    assert lens == [255] * (n_match - 1) + [E - p - 255 * (n_match - 1)]
+    assert all(t[2] == p for t in toks[p:])
+
+
+def _collision_free_period(orc, P, E, seed):
+    """P distinct random words whose P cyclic two-word keys hash to distinct
+    buckets, so every hashed lookup of a periodic chunk is unambiguous."""
+    bits = orc.hash_bits(E)
+    rng = np.random.default_rng(seed)
+    while True:
+        base = rng.integers(1, 2**32, P, dtype=np.uint64).astype(np.uint32)
+        if len(set(base.tolist())) < P:
+            continue
+        keys = {orc.hash2(int(base[j]), int(base[(j + 1) % P]), bits) for j in range(P)}
+        if len(keys) == P:
+            return base
+
+
+def test_period40_level1_closed_form(orc):
+    """Period 40 > 32: the near window sees nothing. Level 1 finds a candidate
+    at position i only for sources in earlier sub-blocks (of 64 positions), and
+    the bucket keeps the most recent (largest) position:
+      i = 0..63   : sub-block 0 looks up an empty table -> 64 literals
+      i = 64      : most recent key position in [0, 64) is 24 -> (255, 40)
+      i = 319     : sub-block 4, table holds [0, 256): most recent of
+                    39, 79, ..., 239 is 239 -> offset 80, length 512-319 = 193.
+    """
+    E, P = 512, 40
+    base = _collision_free_period(orc, P, E, 4040)
+    w = np.tile(base, E // P + 1)[:E]
+    x = w.view(np.uint8)
+    blk0, items0, d0 = orc.encode_chunk(x, 4, 2048, 0)
+    assert items0 == 0x80000000 and d0 == 2048          # level 0: raw
+    blk, items, dbytes = orc.encode_chunk(x, 4, 2048, 1)
+    assert items == 66 and dbytes == 64 * 4 + 4
+    assert blk.size == 12 + 260
+    fl = blk[:12].view(np.uint32)
+    assert list(fl) == [0, 0, 0b11]
+    data = blk[12:]
+    assert np.array_equal(data[:256].view(np.uint32), w[:64])
+    assert list(data[256:260]) == [255, 40, 193, 80]
+
+
+def test_level1_never_worse_than_level0_and_valid(orc):
+    rng = np.random.default_rng(7)
+    for E in (256, 512, 1024):
+        for alphabet in (3, 50, 1000):
+            w = rng.integers(0, alphabet, E).astype(np.uint32)
+            L0, O0 = orc.near_matches(w)
+            L1, O1 = orc.level1_matches(w)
+            assert (L1 >= L0).all()
+            for i in range(E):
+                if L1[i]:
+                    o, ln = int(O1[i]), int(L1[i])
+                    assert 1 <= o <= min(255, i)
+                    assert np.array_equal(w[i:i + ln], w[i - o:i - o + ln])
+                    if L1[i] == L0[i]:
+                        assert O1[i] == O0[i]
+
+
+def test_level1_table_definition_tiny(orc):
+    """Declarative form of the sub-block rule on small chunks: the candidate for
+    i in sub-block s is the largest p < s*E/8 (p+1 < E) whose two-word key
+    hashes to i's bucket; it counts only if it verifies and i - p <= 255."""
+    rng = np.random.default_rng(11)
+    for E in (256, 512):
+        bits = orc.hash_bits(E)
+        for alphabet in (2, 4, 9):
+            w = rng.integers(0, alphabet, E).astype(np.uint32)
+            L0, O0 = orc.near_matches(w)
+            L1, O1 = orc.level1_matches(w)
+            h = [orc.hash2(int(w[p]), int(w[p + 1]), bits) for p in range(E - 1)]
+            sb = E // 8
+            for i in range(E - 1):
+                s = i // sb
+                cands = [p for p in range(0, s * sb) if p + 1 < E and h[p] == h[i]]
+                el, eo = int(L0[i]), int(O0[i])
+                if cands:
+                    p = max(cands)
+                    d = i - p
+                    if 1 <= d <= 255:
+                        k = 0
+                        cap = min(255, E - i)
+                        while k < cap and w[i + k] == w[p + k]:
+                            k += 1
+                        if k > el or (k == el and k > 0 and d < eo):
+                            el, eo = k, d
+                assert (L1[i], O1[i]) == (el, eo), (E, alphabet, i)
+
+
+def _one_chunk_stream(orc, x, ws, cs, lvl):
+    return orc.compress(x, ws, cs, lvl)
+
+
+def test_zero_chunk_sentinel_and_raw(orc):
+    g = [c for c in goldens.load_all() if c["name"].startswith("zero_then")][0]
+    s = orc.compress(g["x"], 4, 1024, 0)
+    assert np.array_equal(s, g["stream"])
+
+
+# ----------------------------------------------------------------------------
+# golden streams
+# ----------------------------------------------------------------------------
+@pytest.mark.parametrize("case", goldens.load_all(), ids=lambda c: c["name"])
+def test_golden_streams(orc, case):
+    for lvl in case["levels"]:
+        s = orc.compress(case["x"], case["ws"], case["cs"], lvl)
+        assert np.array_equal(s, case["stream"]), lvl
+    y = orc.decompress(case["stream"], case["x"].size)
+    assert np.array_equal(y, case["x"])
+    p = streamcheck.check_invariants(case["stream"], case["x"].size)
+    assert np.array_equal(streamcheck.replay(p), case["x"])
+
+
+# ----------------------------------------------------------------------------
+# invariants + round trip
+# ----------------------------------------------------------------------------
+GEOMS = [(ws, cs) for ws in (1, 2, 4) for cs in (1024, 2048, 4096)]
+
+
+@pytest.mark.parametrize("ws,cs", GEOMS)
+@pytest.mark.parametrize("lvl", [0, 1])
+def test_round_trip_and_invariants_random(orc, ws, cs, lvl):
+    rng = np.random.default_rng(ws * 100 + cs + lvl)
+    for n in (0, 1, 3, cs - 1, cs, cs + 1, 3 * cs + 5, 7 * cs + 2):
+        kind = rng.integers(0, 4)
+        if kind == 0:
+            x = rng.integers(0, 4, n).astype(np.uint8)
+        elif kind == 1:
+            x = rng.integers(0, 256, n).astype(np.uint8)
+        elif kind == 2:
+            x = np.zeros(n, np.uint8)
+            if n:
+                x[rng.integers(0, n, n // 50 + 1)] = 3
+        else:
+            x = (np.arange(n) // 7 % 5).astype(np.uint8)
+        s = orc.compress(x, ws, cs, lvl)
+        p = streamcheck.check_invariants(s, n)
+        assert np.array_equal(streamcheck.replay(p), x)
+        assert np.array_equal(orc.decompress(s, n), x)
+        assert s.size <= orc.compress_bound(n, ws, cs)
+
+
+@pytest.mark.parametrize("cfg_id", [1])
+@pytest.mark.parametrize("lvl", [0, 1])
+def test_round_trip_tiny_workload(orc, cfg_id, lvl):
+    import synth
+    cfg = synth.CONFIGS[cfg_id]
+    x = synth.generate(cfg_id)
+    s = orc.compress(x, cfg.word_size, cfg.chunk_size, lvl)
+    p = streamcheck.check_invariants(s, x.size)
+    assert np.array_equal(orc.decompress(s, x.size), x)
+    assert np.array_equal(streamcheck.replay(p), x)
+
+
+def test_levels_decode_identically_plane(orc):
+    import synth
+    x = synth.generate(2)[: 1 << 21]
+    s0 = orc.compress(x, 4, 2048, 0)
+    s1 = orc.compress(x, 4, 2048, 1)
+    assert s1.size <= s0.size
+    assert np.array_equal(orc.decompress(s0, x.size), x)
+    assert np.array_equal(orc.decompress(s1, x.size), x)
+
+
+def test_threaded_oracle_matches_sequential(orc):
+    import synth
+    x = synth.generate(1)
+    for lvl in (0, 1):
+        a = orc.compress(x, 4, 2048, lvl)
+        b = orc.compress_threads(x, 4, 2048, lvl, threads=4)
+        assert np.array_equal(a, b)
+
+
+# ----------------------------------------------------------------------------
+# decoder rejects corrupt streams
+# ----------------------------------------------------------------------------
+def test_oracle_decoder_rejects_corruption(orc):
+    import synth
+    x = synth.generate(1)[:20000]
+    s = orc.compress(x, 4, 2048, 0)
+    assert orc.decompress_status(s, x.size) == 0
+    assert orc.decompress_status(s[:-4], x.size) != 0          # truncated
+    assert orc.decompress_status(s, x.size + 1) != 0           # wrong n
+    bad = s.copy()
+    bad[0] ^= 1                                               # magic
+    assert orc.decompress_status(bad, x.size) != 0
+    bad = s.copy()
+    bad[32 + 4] ^= 0x40                                        # data_bytes of chunk 0
+    assert orc.decompress_status(bad, x.size) != 0
