@@ -1,0 +1,422 @@
+#!/usr/bin/env python3
+"""Benchmark of the GPULZ coder on GB300: one step = encode + decode of one
+1800x3600 uint32 Lorenzo-code field (25.92 MB, chunk_size 2048, word_size 4,
+match level 0), inputs resident in HBM.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Prints ONE JSON line (rank 0). With N > 1 (torchrun), every rank codes its own
+copy of the workload (weak scaling, no data-path collective); the timed region
+is bracketed by a barrier + synchronize and the max over ranks is taken.
+
+--impl reference times the CPU oracle (the plain sequential C coder, spread
+over the host's cores by chunk range) on the same workload and metric.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "GPULZ encode+decode round-trip throughput (uncompressed GB/s)"
+UNIT = "GB/s"
+CFG_ID = 2
+L2_FLUSH_BYTES = 256 << 20  # > 129 MB L2
+FALLBACK_HBM_GBS = 6800.0
+
+
+def log(*a):
+    print(*a, file=sys.stderr, flush=True)
+
+
+def parse_args():
+    p = argparse.ArgumentParser()
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=30)
+    p.add_argument("--warmup", type=int, default=5)
+    p.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    p.add_argument("--config", type=int, default=CFG_ID)
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--no-e2e", action="store_true")
+    return p.parse_args()
+
+
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def workload_config(cfg):
+    return {
+        "workload": cfg.name,
+        "field": "x".join(str(s) for s in cfg.shape) + " float32 sinusoids+noise, "
+                 + cfg.lorenzo + " Lorenzo codes (" + cfg.dtype + ", radius %d)" % cfg.radius,
+        "n_bytes": cfg.n_bytes,
+        "word_size": cfg.word_size,
+        "chunk_size": cfg.chunk_size,
+        "match_level": cfg.match_level,
+        "seed": cfg.seed,
+        "l2": "flushed between timed steps (256 MB write)",
+    }
+
+
+# ----------------------------------------------------------------------------
+# clocks sampler
+# ----------------------------------------------------------------------------
+class ClockSampler:
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), "--query-gpu=" + self.QUERY,
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *exc):
+        self.lines = []
+        if self.proc is not None:
+            time.sleep(0.25)
+            self.proc.terminate()
+            try:
+                out, _ = self.proc.communicate(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+                out, _ = self.proc.communicate()
+            self.lines = [ln for ln in out.splitlines() if ln.strip()]
+        return False
+
+    def summary(self):
+        sm, smax, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in getattr(self, "lines", []):
+            f = [v.strip() for v in ln.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                smax = float(f[2])
+            except ValueError:
+                continue
+            for nm, v in zip(names, f[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(nm)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": smax,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ----------------------------------------------------------------------------
+# helpers
+# ----------------------------------------------------------------------------
+def measured_peak():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            return float(json.load(f)["hbm_gbs"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def kernel_source_sha():
+    h = hashlib.sha256()
+    for name in ("gpulz_encode.cu", "gpulz_decode.cu", "gpulz_internal.cuh"):
+        with open(os.path.join(ROOT, "lz77_family_coder_gb300", "csrc", name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(kernel: str, workload: str):
+    """DRAM bytes per launch from a committed ncu summary, if the kernel
+    sources are unchanged since it was taken."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(path) as f:
+            rec = json.load(f)
+    except (OSError, ValueError):
+        return None
+    r = rec.get(kernel, {})
+    if r.get("workload") != workload or r.get("source_sha") != kernel_source_sha():
+        return None
+    return r.get("dram_bytes_per_launch")
+
+
+def cpu_baseline(x, cfg, reps=3):
+    import oracle
+    threads = os.cpu_count() or 1
+    times = []
+    for _ in range(reps):
+        t0 = time.perf_counter()
+        s = oracle.compress_threads(x, cfg.word_size, cfg.chunk_size, cfg.match_level, threads)
+        y = oracle.decompress_threads(s, x.size, threads)
+        times.append(time.perf_counter() - t0)
+    assert (y == x).all()
+    t = statistics.median(times)
+    return {"value": round(x.size / t / 1e9, 4), "unit": UNIT, "cores": threads,
+            "kind": "oracle",
+            "sample": "whole workload (%d bytes), encode+decode round trip, median of %d"
+                      % (x.size, reps)}
+
+
+# ----------------------------------------------------------------------------
+# our arm
+# ----------------------------------------------------------------------------
+def run_ours(args):
+    import numpy as np
+    import torch
+    import torch.distributed as dist
+
+    import lz77_family_coder_gb300 as g
+    import synth
+
+    world, rank, local = dist_env()
+    if world > 1:
+        dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    g.load()  # raises if the CUDA library is missing: no fallback
+    cfg = synth.CONFIGS[args.config]
+    ws, cs, lvl = cfg.word_size, cfg.chunk_size, cfg.match_level
+    x = synth.generate(cfg)
+    n = x.size
+    d_in = torch.from_numpy(x).to(dev)
+    cap = g.gpulz_compress_bound(n, ws, cs)
+    out = torch.empty(cap, dtype=torch.uint8, device=dev)
+    nb = torch.zeros(1, dtype=torch.int64, device=dev)
+    y = torch.empty(n, dtype=torch.uint8, device=dev)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    sh = stream.cuda_stream
+
+    def step():
+        st = g.gpulz_compress(d_in, n, ws, cs, lvl, out, cap, nb, sh)
+        assert st == g.GPULZ_OK, st
+        st = g.gpulz_decompress(out, y, n, sh)
+        assert st == g.GPULZ_OK, st
+
+    for _ in range(max(args.warmup, 3)):
+        flush.fill_(1)
+        step()
+    assert g.gpulz_device_status(sh) == g.GPULZ_OK
+    torch.cuda.synchronize()
+
+    K = args.steps
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True),
+           torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clocks:
+        for k in range(K):
+            flush.fill_(k & 0xFF)  # evict the input from L2 (outside the events)
+            ev[k][0].record(stream)
+            assert g.gpulz_compress(d_in, n, ws, cs, lvl, out, cap, nb, sh) == g.GPULZ_OK
+            ev[k][1].record(stream)
+            assert g.gpulz_decompress(out, y, n, sh) == g.GPULZ_OK
+            ev[k][2].record(stream)
+        torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    t_enc = [a.elapsed_time(b) for a, b, c in ev]
+    t_dec = [b.elapsed_time(c) for a, b, c in ev]
+    total_ms = sum(t_enc) + sum(t_dec)
+    if world > 1:
+        tt = torch.tensor([total_ms], dtype=torch.float64, device=dev)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        total_ms = float(tt.item())
+    status = g.gpulz_device_status(sh)
+
+    # parity after timing, on the same buffers
+    S = int(nb.item())
+    stream_host = out[:S].cpu().numpy()
+    parity = "unchecked"
+    if rank == 0:
+        import oracle
+        ref = oracle.compress_threads(x, ws, cs, lvl, os.cpu_count() or 1)
+        ok = np.array_equal(stream_host, ref) and np.array_equal(y.cpu().numpy(), x)
+        parity = "bit-exact vs oracle" if ok and status == 0 else "MISMATCH"
+
+    # end to end through the C ABI with host buffers
+    e2e = None
+    if not args.no_e2e:
+        h_x = torch.from_numpy(x).pin_memory()
+        h_nb = torch.zeros(1, dtype=torch.int64).pin_memory()
+        h_s = torch.empty(cap, dtype=torch.uint8).pin_memory()
+        h_y = torch.empty(n, dtype=torch.uint8).pin_memory()
+        d_s = torch.empty(cap, dtype=torch.uint8, device=dev)
+
+        def e2e_step():
+            d_in.copy_(h_x, non_blocking=True)
+            assert g.gpulz_compress(d_in, n, ws, cs, lvl, out, cap, nb, sh) == g.GPULZ_OK
+            h_nb.copy_(nb, non_blocking=True)
+            stream.synchronize()
+            s_len = int(h_nb[0])
+            h_s[:s_len].copy_(out[:s_len], non_blocking=True)
+            d_s[:s_len].copy_(h_s[:s_len], non_blocking=True)
+            assert g.gpulz_decompress(d_s, y, n, sh) == g.GPULZ_OK
+            h_y.copy_(y, non_blocking=True)
+            stream.synchronize()
+            return s_len
+
+        for _ in range(3):
+            e2e_step()
+        if world > 1:
+            dist.barrier()
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        s_len = 0
+        for _ in range(K):
+            s_len = e2e_step()
+        torch.cuda.synchronize()
+        t_e2e = time.perf_counter() - t0
+        if world > 1:
+            tt = torch.tensor([t_e2e], dtype=torch.float64, device=dev)
+            dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+            t_e2e = float(tt.item())
+        assert torch.equal(h_y, h_x)
+        e2e = {"value": round(world * n * K / t_e2e / 1e9, 3), "unit": UNIT,
+               "h2d_bytes_per_step": n + s_len, "d2h_bytes_per_step": 8 + s_len + n,
+               "path": "pinned host -> gpulz_compress -> host stream -> gpulz_decompress -> host"}
+
+    if rank != 0:
+        if world > 1:
+            dist.destroy_process_group()
+        return
+
+    enc_ms = statistics.mean(t_enc)
+    dec_ms = statistics.mean(t_dec)
+    peak, peak_kind = measured_peak()
+    enc_alg = n + S
+    dec_alg = S + n
+    dominant = "encode_kernel" if enc_ms >= dec_ms else "decode_kernel"
+    dom_ms = max(enc_ms, dec_ms)
+    achieved = (enc_alg if dominant == "encode_kernel" else dec_alg) / (dom_ms * 1e-3) / 1e9
+    roofline = {
+        "kernel": dominant, "bound": "hbm", "achieved": round(achieved, 2),
+        "peak": peak, "unit": "GB/s", "frac": round(achieved / peak, 4),
+        "peak_source": peak_kind + " (MEASURED_PEAKS.json hbm_gbs, burst copy)",
+        "traffic": recorded_traffic(dominant, cfg.name),
+        "algorithmic_bytes_per_launch": enc_alg if dominant == "encode_kernel" else dec_alg,
+        "encode": {"ms": round(enc_ms, 5), "alg_bytes": enc_alg,
+                   "achieved_gbs": round(enc_alg / (enc_ms * 1e-3) / 1e9, 2),
+                   "frac": round(enc_alg / (enc_ms * 1e-3) / 1e9 / peak, 4)},
+        "decode": {"ms": round(dec_ms, 5), "alg_bytes": dec_alg,
+                   "achieved_gbs": round(dec_alg / (dec_ms * 1e-3) / 1e9, 2),
+                   "frac": round(dec_alg / (dec_ms * 1e-3) / 1e9 / peak, 4)},
+    }
+    line = {
+        "metric": METRIC,
+        "value": round(world * n * K / (total_ms * 1e-3) / 1e9, 3),
+        "unit": UNIT,
+        "n_gpus": world,
+        "steps": K,
+        "warmup": max(args.warmup, 3),
+        "ms_per_step": round(total_ms / K, 5),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": cfg.dtype,
+        "data": "synthetic (seeded stand-in for Lorenzo-quantized CLDHGH residuals)",
+        "config": workload_config(cfg),
+        "encode_gbs": round(n / (enc_ms * 1e-3) / 1e9, 2),
+        "decode_gbs": round(n / (dec_ms * 1e-3) / 1e9, 2),
+        "ratio": round(n / S, 4),
+        "stream_bytes": S,
+        "parity": parity,
+        "device_status": status,
+        "roofline": roofline,
+        "gpu_launches": 2 * K,
+        "clocks": clocks.summary(),
+        "e2e": e2e,
+    }
+    if not args.no_cpu_baseline and world == 1:
+        line["cpu_baseline"] = cpu_baseline(x, cfg)
+    print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+
+
+# ----------------------------------------------------------------------------
+# reference arm: the CPU oracle on the host cores
+# ----------------------------------------------------------------------------
+def run_reference(args):
+    world, rank, local = dist_env()
+    if rank != 0:
+        return
+    import oracle
+    import synth
+    cfg = synth.CONFIGS[args.config]
+    x = synth.generate(cfg)
+    threads = os.cpu_count() or 1
+
+    def step():
+        s = oracle.compress_threads(x, cfg.word_size, cfg.chunk_size, cfg.match_level, threads)
+        y = oracle.decompress_threads(s, x.size, threads)
+        return s, y
+
+    for _ in range(max(args.warmup, 3)):
+        s, y = step()
+    assert (y == x).all()
+    times = []
+    for _ in range(args.steps):
+        t0 = time.perf_counter()
+        s, y = step()
+        times.append(time.perf_counter() - t0)
+    total = sum(times)
+    value = round(x.size * args.steps / total / 1e9, 4)
+    line = {
+        "impl": "reference",
+        "metric": METRIC,
+        "value": value,
+        "unit": UNIT,
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": max(args.warmup, 3),
+        "ms_per_step": round(total * 1e3 / args.steps, 3),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": cfg.dtype,
+        "data": "synthetic (seeded stand-in for Lorenzo-quantized CLDHGH residuals)",
+        "config": workload_config(cfg),
+        "ratio": round(x.size / s.size, 4),
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": threads, "kind": "oracle",
+                         "sample": "whole workload per step (%d bytes), encode+decode round trip"
+                                   % x.size},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    args = parse_args()
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,133 @@
+/*
+ * gpulz.h -- C ABI of the GB300 (sm_103a) GPULZ chunked LZSS coder.
+ *
+ * The coder is the one described by the FZGPUModules GPULZ stage
+ * documentation ("fz::GPULZStage", stage_gpulz page) and its codebase note
+ * CN-GPULZ-1: the input is split into fixed chunk_size-byte chunks of
+ * word_size-byte elements; each chunk is coded on its own into literal words
+ * and 2-byte [length, offset] match tokens plus a literal/match flag bitmap
+ * (class summary); level 0 searches the 32-element near window exactly with
+ * ANDed equality masks, level 1 adds hashed two-word-key candidates with
+ * offsets up to 255 over 8 sub-blocks (match-search section); a chunk whose
+ * coded form is not smaller is stored raw (raw-fallback paragraph); an all-zero
+ * chunk costs only its size-table entry (zero-chunk paragraph); decode is
+ * block-parallel (scan of item sizes, pointer jumping over back-references).
+ *
+ * Stream format v1 (little-endian, every padding byte zero):
+ *   header, 32 bytes : u32 magic 0x5A4C5047 ("GPLZ"), u16 version = 1,
+ *                      u8 word_size, u8 reserved = 0, u32 chunk_size,
+ *                      u32 n_chunks, u64 orig_bytes, u64 stream_bytes
+ *   size table       : n_chunks x { u32 n_items | RAW << 31, u32 data_bytes }
+ *                      zero chunk = {0, 0}; raw chunk = {RAW, chunk_size}
+ *   blocks, in chunk order, each a multiple of 4 bytes:
+ *     normal : u32 flags[ceil(n_items/32)] (bit j of word j/32, 1 = match),
+ *              then the items (literal = word_size bytes as in the input,
+ *              match = u8 length, u8 offset, both in elements), zero padded
+ *     raw    : chunk_size bytes of the zero-padded chunk
+ *     zero   : nothing
+ * The match level is not recorded: streams from either level decode alike.
+ *
+ * Supported geometry: word_size in {1, 2, 4}, chunk_size in {1024, 2048,
+ * 4096} (elements per chunk = chunk_size / word_size, a power of two >= 256).
+ *
+ * Memory: every d_* pointer is device memory owned by the caller. The library
+ * owns only a small per-(device, stream) scratch area (look-back descriptors,
+ * 8 bytes per chunk, ticket counters and a status word). The first call on a
+ * stream, or a call with more chunks than any earlier call on it, allocates
+ * that scratch (stream-ordered); later calls allocate nothing.
+ *
+ * Errors: argument errors a host can check are returned synchronously and
+ * nothing is launched. Conditions found on the device (corrupt stream, size
+ * mismatch, output capacity exceeded, look-back wait timeout) are recorded in
+ * the stream's device status word, read and cleared by gpulz_device_status().
+ * The kernels never trap.
+ */
+#ifndef GPULZ_H
+#define GPULZ_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum gpulz_status {
+    GPULZ_OK = 0,
+    GPULZ_ERR_INVALID_ARG = 1,   /* bad pointer / geometry / level; nothing launched */
+    GPULZ_ERR_CAPACITY = 2,      /* compressed stream did not fit in `capacity` */
+    GPULZ_ERR_CORRUPT = 3,       /* stream fails validation while decoding */
+    GPULZ_ERR_TIMEOUT = 4,       /* a bounded device-side wait gave up */
+    GPULZ_ERR_CUDA = 5,          /* a CUDA runtime call failed */
+    GPULZ_ERR_SIZE_MISMATCH = 6  /* n_bytes differs from the stream's original size */
+} gpulz_status;
+
+/*
+ * gpulz_compress -- encode n_bytes at d_in into one GPULZ stream at d_out.
+ * (GPULZ stage page: class summary, match-search section, raw-fallback and
+ * zero-chunk paragraphs; graph-capture paragraph for the deferred size.)
+ *
+ *   d_in        device, n_bytes bytes, any alignment (16-byte alignment takes
+ *               the vector-load path). May be NULL only if n_bytes == 0.
+ *   word_size   1, 2 or 4: element width in bytes.
+ *   chunk_size  1024, 2048 or 4096: bytes per independently coded chunk. The
+ *               last chunk is zero padded (the padding is coded like data).
+ *   match_level 0 = exact near window only; 1 = plus hashed candidates.
+ *   d_out       device buffer of `capacity` bytes. Nothing is written at or
+ *               past d_out + capacity. capacity >= gpulz_compress_bound()
+ *               always suffices.
+ *   d_out_bytes device pointer to one size_t that receives the stream length
+ *               (the length needed, if it exceeds capacity; then the device
+ *               status also records GPULZ_ERR_CAPACITY).
+ *   stream      CUDA stream; the call only enqueues work on it.
+ * Returns GPULZ_OK once the work is enqueued.
+ */
+gpulz_status gpulz_compress(const void* d_in, size_t n_bytes, int word_size, int chunk_size,
+                            int match_level, void* d_out, size_t capacity, size_t* d_out_bytes,
+                            cudaStream_t stream);
+
+/*
+ * gpulz_decompress -- decode the GPULZ stream at d_in into n_bytes at d_out.
+ * (GPULZ stage page: decode paragraph -- one scan recovers every item's
+ * offset, each element points back to q - offset, pointer jumping for
+ * log2(elements) rounds; zero-chunk and raw-fallback paragraphs.)
+ *
+ *   d_in    device, the whole stream. The header's stream_bytes bytes must be
+ *           readable; use gpulz_decompress_bounded() when the buffer length
+ *           is known and the stream is untrusted.
+ *   d_out   device, n_bytes bytes, written only in [d_out, d_out + n_bytes).
+ *   n_bytes the original length; a header that disagrees records
+ *           GPULZ_ERR_SIZE_MISMATCH and nothing is written.
+ * The header is parsed on the device: no host synchronisation, so the call
+ * can be captured into a CUDA graph once the stream's scratch exists.
+ */
+gpulz_status gpulz_decompress(const void* d_in, void* d_out, size_t n_bytes, cudaStream_t stream);
+
+/* As gpulz_decompress, but no byte at or past d_in + in_bytes is read: a
+ * header or size table that points further records GPULZ_ERR_CORRUPT. */
+gpulz_status gpulz_decompress_bounded(const void* d_in, size_t in_bytes, void* d_out,
+                                      size_t n_bytes, cudaStream_t stream);
+
+/* Worst-case stream length: 32 + n_chunks * (8 + chunk_size) (every chunk
+ * raw). Host only; returns 0 for an unsupported geometry. */
+size_t gpulz_compress_bound(size_t n_bytes, int word_size, int chunk_size);
+
+/* Parse a stream header copied to host memory (h_len >= 32). Host only. Any
+ * output pointer may be NULL. */
+gpulz_status gpulz_stream_info(const void* h_header, size_t h_len, size_t* orig_bytes,
+                               size_t* stream_bytes, int* word_size, int* chunk_size);
+
+/* Synchronise `stream`, return the first error recorded by the device since
+ * the last call (GPULZ_OK if none) and clear it. */
+gpulz_status gpulz_device_status(cudaStream_t stream);
+
+/* Static, human-readable name of a status code. */
+const char* gpulz_status_string(gpulz_status status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* GPULZ_H */

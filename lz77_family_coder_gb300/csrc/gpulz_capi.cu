@@ -1,0 +1,213 @@
+// C ABI of the GPULZ coder: argument checks, per-(device, stream) scratch,
+// launches and the device status word. The kernels live in gpulz_encode.cu and
+// gpulz_decode.cu.
+#include <cuda_runtime.h>
+#include <stdint.h>
+#include <string.h>
+
+#include <mutex>
+#include <vector>
+
+#include "../../include/gpulz.h"
+#include "gpulz_internal.cuh"
+
+namespace {
+
+using namespace gpulz;
+
+// Scratch of one (device, stream): status word, one ticket counter per epoch,
+// look-back descriptors. A call takes the next epoch; descriptors and tickets
+// of other epochs never match, so nothing is cleared between calls. When the
+// 16-bit epoch wraps, the whole area is cleared once on the stream.
+struct Scratch {
+    int device;
+    cudaStream_t stream;
+    uint8_t* base;
+    uint64_t desc_capacity;  // chunks
+    uint32_t epoch;          // last epoch used
+};
+
+std::mutex g_mu;
+std::vector<Scratch*> g_scratch;
+
+size_t scratch_bytes(uint64_t chunks) { return kDescOffset + sizeof(uint64_t) * chunks; }
+
+// Returns the scratch for (current device, stream) with room for `chunks`
+// descriptors and advances its epoch; *epoch_out receives the epoch to use.
+cudaError_t acquire_scratch(cudaStream_t stream, uint64_t chunks, Scratch** out,
+                            uint32_t* epoch_out) {
+    int dev = 0;
+    cudaError_t err = cudaGetDevice(&dev);
+    if (err != cudaSuccess) return err;
+    std::lock_guard<std::mutex> lock(g_mu);
+    Scratch* s = nullptr;
+    for (Scratch* t : g_scratch)
+        if (t->device == dev && t->stream == stream) s = t;
+    if (s == nullptr) {
+        s = new Scratch{dev, stream, nullptr, 0, 0};
+        g_scratch.push_back(s);
+    }
+    if (s->base == nullptr || s->desc_capacity < chunks) {
+        uint64_t cap = chunks < 4096 ? 4096 : chunks;
+        void* p = nullptr;
+        if ((err = cudaMallocAsync(&p, scratch_bytes(cap), stream)) != cudaSuccess) return err;
+        if ((err = cudaMemsetAsync(p, 0, scratch_bytes(cap), stream)) != cudaSuccess) return err;
+        if (s->base != nullptr) {
+            // keep recorded errors; earlier work on this stream still owns the old area,
+            // so it is released in stream order
+            if ((err = cudaMemcpyAsync(p, s->base, sizeof(uint32_t), cudaMemcpyDeviceToDevice,
+                                       stream)) != cudaSuccess)
+                return err;
+            if ((err = cudaFreeAsync(s->base, stream)) != cudaSuccess) return err;
+            s->base = nullptr;
+        }
+        s->base = static_cast<uint8_t*>(p);
+        s->desc_capacity = cap;
+        s->epoch = 0;
+    }
+    s->epoch += 1;
+    if (s->epoch >= kEpochs) {
+        // clear tickets and descriptors (keep the status word)
+        if ((err = cudaMemsetAsync(s->base + kTicketOffset, 0,
+                                   scratch_bytes(s->desc_capacity) - kTicketOffset, stream)) !=
+            cudaSuccess)
+            return err;
+        s->epoch = 1;
+    }
+    *out = s;
+    *epoch_out = s->epoch;
+    return cudaSuccess;
+}
+
+Scratch* find_scratch(cudaStream_t stream) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return nullptr;
+    std::lock_guard<std::mutex> lock(g_mu);
+    for (Scratch* t : g_scratch)
+        if (t->device == dev && t->stream == stream && t->base) return t;
+    return nullptr;
+}
+
+inline bool aligned(const void* p, uintptr_t a) {
+    return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0;
+}
+
+}  // namespace
+
+extern "C" {
+
+size_t gpulz_compress_bound(size_t n_bytes, int word_size, int chunk_size) {
+    if (!valid_geometry(word_size, chunk_size)) return 0;
+    uint64_t chunks = ((uint64_t)n_bytes + (uint64_t)chunk_size - 1) / (uint64_t)chunk_size;
+    return (size_t)(kHeaderBytes + chunks * ((uint64_t)kEntryBytes + (uint64_t)chunk_size));
+}
+
+gpulz_status gpulz_compress(const void* d_in, size_t n_bytes, int word_size, int chunk_size,
+                            int match_level, void* d_out, size_t capacity, size_t* d_out_bytes,
+                            cudaStream_t stream) {
+    if (!valid_geometry(word_size, chunk_size)) return GPULZ_ERR_INVALID_ARG;
+    if (match_level != 0 && match_level != 1) return GPULZ_ERR_INVALID_ARG;
+    if ((n_bytes > 0 && d_in == nullptr) || d_out == nullptr || d_out_bytes == nullptr)
+        return GPULZ_ERR_INVALID_ARG;
+    if (!aligned(d_out, 4) || !aligned(d_out_bytes, 8)) return GPULZ_ERR_INVALID_ARG;
+    const uint64_t chunks = ((uint64_t)n_bytes + chunk_size - 1) / (uint64_t)chunk_size;
+    if (chunks > 0xFFFFFFFFull) return GPULZ_ERR_INVALID_ARG;
+    Scratch* s = nullptr;
+    uint32_t epoch = 0;
+    if (acquire_scratch(stream, chunks, &s, &epoch) != cudaSuccess) return GPULZ_ERR_CUDA;
+    EncodeArgs a;
+    a.in = static_cast<const uint8_t*>(d_in);
+    a.n_bytes = n_bytes;
+    a.out = static_cast<uint8_t*>(d_out);
+    a.capacity = capacity;
+    a.out_bytes = reinterpret_cast<unsigned long long*>(d_out_bytes);
+    a.desc = reinterpret_cast<uint64_t*>(s->base + kDescOffset);
+    a.ticket = reinterpret_cast<uint32_t*>(s->base + kTicketOffset) + epoch;
+    a.status = reinterpret_cast<uint32_t*>(s->base);
+    a.epoch = epoch;
+    a.chunk_size = (uint32_t)chunk_size;
+    a.elems = (uint32_t)(chunk_size / word_size);
+    a.n_chunks = (uint32_t)chunks;
+    a.hash_bits = log2_exact(2u * a.elems);
+    if (launch_encode(a, word_size, match_level, stream) != cudaSuccess) return GPULZ_ERR_CUDA;
+    return GPULZ_OK;
+}
+
+gpulz_status gpulz_decompress_bounded(const void* d_in, size_t in_bytes, void* d_out,
+                                      size_t n_bytes, cudaStream_t stream) {
+    if (d_in == nullptr || (n_bytes > 0 && d_out == nullptr)) return GPULZ_ERR_INVALID_ARG;
+    if (!aligned(d_in, 4)) return GPULZ_ERR_INVALID_ARG;
+    const uint64_t max_chunks = ((uint64_t)n_bytes + 1023u) / 1024u;
+    Scratch* s = nullptr;
+    uint32_t epoch = 0;
+    if (acquire_scratch(stream, max_chunks, &s, &epoch) != cudaSuccess) return GPULZ_ERR_CUDA;
+    DecodeArgs a;
+    a.in = static_cast<const uint8_t*>(d_in);
+    a.in_bytes = in_bytes;
+    a.out = static_cast<uint8_t*>(d_out);
+    a.n_bytes = n_bytes;
+    a.desc = reinterpret_cast<uint64_t*>(s->base + kDescOffset);
+    a.ticket = reinterpret_cast<uint32_t*>(s->base + kTicketOffset) + epoch;
+    a.status = reinterpret_cast<uint32_t*>(s->base);
+    a.epoch = epoch;
+    if (launch_decode(a, stream) != cudaSuccess) return GPULZ_ERR_CUDA;
+    return GPULZ_OK;
+}
+
+gpulz_status gpulz_decompress(const void* d_in, void* d_out, size_t n_bytes, cudaStream_t stream) {
+    return gpulz_decompress_bounded(d_in, SIZE_MAX, d_out, n_bytes, stream);
+}
+
+gpulz_status gpulz_stream_info(const void* h_header, size_t h_len, size_t* orig_bytes,
+                               size_t* stream_bytes, int* word_size, int* chunk_size) {
+    if (h_header == nullptr || h_len < kHeaderBytes) return GPULZ_ERR_INVALID_ARG;
+    const uint8_t* h = static_cast<const uint8_t*>(h_header);
+    uint32_t w[8];
+    for (int k = 0; k < 8; ++k)
+        w[k] = (uint32_t)h[4 * k] | ((uint32_t)h[4 * k + 1] << 8) | ((uint32_t)h[4 * k + 2] << 16) |
+               ((uint32_t)h[4 * k + 3] << 24);
+    const int ws = (int)((w[1] >> 16) & 0xFFu);
+    const int cs = (int)w[2];
+    const uint64_t orig = (uint64_t)w[4] | ((uint64_t)w[5] << 32);
+    const uint64_t total = (uint64_t)w[6] | ((uint64_t)w[7] << 32);
+    if (w[0] != kMagic || (w[1] & 0xFFFFu) != kVersion || (w[1] >> 24) != 0 ||
+        !valid_geometry(ws, cs))
+        return GPULZ_ERR_CORRUPT;
+    const uint64_t chunks = (orig + (uint64_t)cs - 1) / (uint64_t)cs;
+    if (chunks != w[3] || total < kHeaderBytes + kEntryBytes * chunks) return GPULZ_ERR_CORRUPT;
+    if (orig_bytes) *orig_bytes = (size_t)orig;
+    if (stream_bytes) *stream_bytes = (size_t)total;
+    if (word_size) *word_size = ws;
+    if (chunk_size) *chunk_size = cs;
+    return GPULZ_OK;
+}
+
+gpulz_status gpulz_device_status(cudaStream_t stream) {
+    if (cudaStreamSynchronize(stream) != cudaSuccess) return GPULZ_ERR_CUDA;
+    Scratch* s = find_scratch(stream);
+    if (s == nullptr) return GPULZ_OK;
+    uint32_t bits = 0;
+    if (cudaMemcpy(&bits, s->base, sizeof(bits), cudaMemcpyDeviceToHost) != cudaSuccess)
+        return GPULZ_ERR_CUDA;
+    if (bits != 0 && cudaMemset(s->base, 0, sizeof(bits)) != cudaSuccess) return GPULZ_ERR_CUDA;
+    if (bits & kStatCorrupt) return GPULZ_ERR_CORRUPT;
+    if (bits & kStatSizeMismatch) return GPULZ_ERR_SIZE_MISMATCH;
+    if (bits & kStatTimeout) return GPULZ_ERR_TIMEOUT;
+    if (bits & kStatCapacity) return GPULZ_ERR_CAPACITY;
+    return GPULZ_OK;
+}
+
+const char* gpulz_status_string(gpulz_status status) {
+    switch (status) {
+        case GPULZ_OK: return "ok";
+        case GPULZ_ERR_INVALID_ARG: return "invalid argument";
+        case GPULZ_ERR_CAPACITY: return "output capacity exceeded";
+        case GPULZ_ERR_CORRUPT: return "corrupt stream";
+        case GPULZ_ERR_TIMEOUT: return "device wait timed out";
+        case GPULZ_ERR_CUDA: return "CUDA error";
+        case GPULZ_ERR_SIZE_MISMATCH: return "n_bytes differs from the stream's original size";
+    }
+    return "unknown status";
+}
+
+}  // extern "C"

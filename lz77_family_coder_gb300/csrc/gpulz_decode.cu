@@ -1,0 +1,380 @@
+// GPULZ decode kernel for sm_103a.
+//
+// Block-parallel decode (GPULZ stage page of FZGPUModules, decode paragraph):
+// the flag bitmap fixes every item's byte size (word_size for a literal, 2 for
+// a match), so an item's byte offset follows from a popcount of the flags
+// before it; one warp scan over item spans gives every item's element offset
+// q; each element of a match points back to q - offset (always < q, so chains
+// end) and pointer jumping resolves all of them in at most log2(elements)
+// rounds, stopping early once nothing changes. Zero chunks are zero-filled
+// (zero-chunk paragraph) and raw chunks copied (raw-fallback paragraph).
+//
+// Each warp decodes one chunk at a time, in ticket order, so that a warp's
+// stream offset is the sum of the earlier chunks' block sizes. Those sizes are
+// in the size table, so the look-back never waits: where an earlier chunk has
+// not published its inclusive offset yet, its table entry is read instead.
+//
+// The header is parsed on the device; chunk geometry is not known to the host
+// launcher, so the shared-memory slot per warp is sized from the header at run
+// time and the CTA keeps as many warps as fit.
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "gpulz_internal.cuh"
+
+namespace gpulz {
+namespace {
+
+constexpr uint32_t FULL = 0xFFFFFFFFu;
+constexpr int kDecWarps = 8;
+constexpr uint32_t kDecSmem = 48u * 1024u;
+constexpr int kMaxJumpRounds = 16;
+constexpr uint16_t kLit = 0x8000u;
+
+struct Geo {
+    uint32_t ws, cs, E, C;
+    uint64_t orig, total, body0;
+};
+
+__device__ __forceinline__ uint32_t align16d(uint32_t v) { return (v + 15u) & ~15u; }
+
+// Per-warp shared-memory slot: flags | flag-word prefix | item bytes | src.
+struct DecSlot {
+    uint32_t fl, wp, data, src, total;
+};
+__device__ __forceinline__ DecSlot dec_slot(uint32_t cs, uint32_t E) {
+    DecSlot s;
+    uint32_t o = 0;
+    s.fl = o;   o = align16d(o + E / 8u);
+    s.wp = o;   o = align16d(o + 4u * (E / 32u));
+    s.data = o; o = align16d(o + cs + 16u);
+    s.src = o;  o = align16d(o + 2u * E);
+    s.total = o;
+    return s;
+}
+
+// Block size of a size-table entry; 0xFFFFFFFF if the entry is invalid.
+__device__ __forceinline__ uint32_t entry_block(uint32_t items, uint32_t dbytes, const Geo& g) {
+    if (items == 0 && dbytes == 0) return 0;
+    if (items == kRawBit) return dbytes == g.cs ? g.cs : 0xFFFFFFFFu;
+    if ((items & kRawBit) || items > g.E || dbytes > g.cs) return 0xFFFFFFFFu;
+    uint32_t blk = 4u * ((items + 31u) / 32u) + ((dbytes + 3u) & ~3u);
+    return blk < g.cs ? blk : 0xFFFFFFFFu;
+}
+
+__device__ __forceinline__ uint32_t read_u32(const uint8_t* p) {
+    return *reinterpret_cast<const uint32_t*>(p);
+}
+
+__device__ uint64_t lookback_decode(const DecodeArgs& a, const Geo& g, uint32_t c, uint64_t blk,
+                                    int lane) {
+    uint64_t prefix = 0;
+    int64_t base = (int64_t)c - 1;
+    while (base >= 0) {
+        int64_t idx = base - lane;
+        bool incl = true;
+        uint64_t val = 0;
+        if (idx >= 0) {
+            uint64_t d = ld_relaxed_u64(&a.desc[idx]);
+            incl = desc_epoch(d) == a.epoch && desc_kind(d) == kDescInclusive;
+            val = desc_value(d);
+        }
+        uint32_t m = __ballot_sync(FULL, incl);
+        int f = m ? __ffs(m) - 1 : 32;
+        uint64_t v = 0;
+        if (lane < f && idx >= 0) {
+            const uint8_t* e = a.in + kHeaderBytes + (uint64_t)kEntryBytes * (uint64_t)idx;
+            uint32_t b = entry_block(read_u32(e), read_u32(e + 4), g);
+            v = b == 0xFFFFFFFFu ? 0 : b;
+        } else if (lane == f) {
+            v = val;
+        }
+        prefix += warp_sum_u64(v);
+        if (f < 32) break;
+        base -= 32;
+    }
+    if (lane == 0) st_relaxed_u64(&a.desc[c], make_desc(a.epoch, kDescInclusive, prefix + blk));
+    return prefix;
+}
+
+// Output a chunk as 32-bit words: word j covers chunk bytes [4j, 4j+4).
+template <typename F>
+__device__ __forceinline__ void write_chunk(uint8_t* out, uint32_t take, bool out_aligned, int lane,
+                                            F word_of) {
+    const uint32_t full_words = take / 4u;
+    if (out_aligned) {
+        uint32_t* o = reinterpret_cast<uint32_t*>(out);
+        for (uint32_t j = lane; j < full_words; j += 32) o[j] = word_of(j);
+    } else {
+        for (uint32_t j = lane; j < full_words; j += 32) {
+            uint32_t v = word_of(j);
+            for (int k = 0; k < 4; ++k) out[4u * j + k] = (uint8_t)(v >> (8 * k));
+        }
+    }
+    if (take & 3u) {
+        uint32_t j = full_words;
+        uint32_t v = word_of(j);
+        if (lane < (int)(take & 3u)) out[4u * j + lane] = (uint8_t)(v >> (8 * lane));
+    }
+}
+
+template <int WS>
+__device__ uint32_t lit_word(const uint8_t* s_data, const uint16_t* s_src, uint32_t j) {
+    // chunk bytes [4j, 4j + 4) = elements [4j/WS, (4j+4)/WS)
+    if (WS == 4) {
+        uint32_t b = s_src[j] & 0x7FFFu;
+        return (uint32_t)*reinterpret_cast<const uint16_t*>(s_data + b) |
+               ((uint32_t)*reinterpret_cast<const uint16_t*>(s_data + b + 2) << 16);
+    } else if (WS == 2) {
+        uint32_t b0 = s_src[2 * j] & 0x7FFFu, b1 = s_src[2 * j + 1] & 0x7FFFu;
+        return (uint32_t)*reinterpret_cast<const uint16_t*>(s_data + b0) |
+               ((uint32_t)*reinterpret_cast<const uint16_t*>(s_data + b1) << 16);
+    } else {
+        uint32_t v = 0;
+#pragma unroll
+        for (int k = 0; k < 4; ++k) v |= (uint32_t)s_data[s_src[4 * j + k] & 0x7FFFu] << (8 * k);
+        return v;
+    }
+}
+
+template <int WS>
+__device__ void decode_chunks(const DecodeArgs& a, const Geo& g, uint8_t* slot_base, int lane) {
+    const DecSlot S = dec_slot(g.cs, g.E);
+    uint32_t* s_fl = reinterpret_cast<uint32_t*>(slot_base + S.fl);
+    uint32_t* s_wp = reinterpret_cast<uint32_t*>(slot_base + S.wp);
+    uint8_t* s_data = slot_base + S.data;
+    uint16_t* s_src = reinterpret_cast<uint16_t*>(slot_base + S.src);
+    const uint32_t E = g.E, CS = g.cs;
+    const bool out_aligned = (reinterpret_cast<uintptr_t>(a.out) & 3u) == 0;
+    for (;;) {
+        uint32_t c = 0;
+        if (lane == 0) c = atomicAdd(a.ticket, 1u);
+        c = __shfl_sync(FULL, c, 0);
+        if (c >= g.C) break;
+
+        const uint8_t* e = a.in + kHeaderBytes + (uint64_t)kEntryBytes * c;
+        const uint32_t items = read_u32(e), dbytes = read_u32(e + 4);
+        uint32_t blk = entry_block(items, dbytes, g);
+        bool bad = blk == 0xFFFFFFFFu;
+        const uint64_t prefix = lookback_decode(a, g, c, bad ? 0 : blk, lane);
+        const uint64_t src_off = g.body0 + prefix;
+        if (!bad && src_off + blk > g.total) bad = true;
+        if (c == g.C - 1 && !bad && src_off + blk != g.total) bad = true;
+
+        const uint64_t begin = (uint64_t)c * CS;
+        const uint64_t avail = g.orig - begin;
+        const uint32_t take = avail < CS ? (uint32_t)avail : CS;
+        uint8_t* out = a.out + begin;
+        const bool chunk_out_aligned = out_aligned;
+
+        if (bad) {
+            if (lane == 0) atomicOr(a.status, kStatCorrupt);
+            continue;
+        }
+        if (blk == 0) {
+            write_chunk(out, take, chunk_out_aligned, lane, [](uint32_t) { return 0u; });
+            continue;
+        }
+        const uint8_t* src = a.in + src_off;
+        if (items == kRawBit) {
+            write_chunk(out, take, chunk_out_aligned, lane,
+                        [src](uint32_t j) { return read_u32(src + 4u * j); });
+            continue;
+        }
+
+        // ---- D2: load flags and items into shared memory ----
+        const uint32_t fw = (items + 31u) / 32u;
+        const uint32_t dw = (dbytes + 3u) / 4u;
+        for (uint32_t j = lane; j < fw + dw; j += 32) {
+            uint32_t v = read_u32(src + 4u * j);
+            if (j < fw) {
+                if (j == fw - 1u && (items & 31u)) v &= (1u << (items & 31u)) - 1u;
+                s_fl[j] = v;
+            } else {
+                *reinterpret_cast<uint32_t*>(s_data + 4u * (j - fw)) = v;
+            }
+        }
+        __syncwarp();
+        // flag-word prefix popcounts
+        uint32_t run = 0;
+        for (uint32_t j0 = 0; j0 < fw; j0 += 32) {
+            uint32_t j = j0 + lane;
+            uint32_t pc = j < fw ? __popc(s_fl[j]) : 0u;
+            uint32_t incl = pc;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                uint32_t t = __shfl_up_sync(FULL, incl, o);
+                if (lane >= o) incl += t;
+            }
+            if (j < fw) s_wp[j] = run + incl - pc;
+            run += __shfl_sync(FULL, incl, 31);
+        }
+        const uint32_t n_match = run;
+        if ((uint64_t)WS * (items - n_match) + 2ull * n_match != dbytes) {
+            if (lane == 0) atomicOr(a.status, kStatCorrupt);
+            continue;
+        }
+        __syncwarp();
+
+        // ---- D3: item spans, warp scan -> element offsets ----
+        const uint32_t K = (items + 31u) / 32u;
+        const uint32_t j_lo = lane * K < items ? lane * K : items;
+        const uint32_t j_hi = j_lo + K < items ? j_lo + K : items;
+        uint32_t span_sum = 0;
+        for (uint32_t j = j_lo; j < j_hi; ++j) {
+            uint32_t w = s_fl[j >> 5];
+            bool ism = (w >> (j & 31u)) & 1u;
+            if (ism) {
+                uint32_t pm = s_wp[j >> 5] + __popc(w & ((1u << (j & 31u)) - 1u));
+                uint32_t b = WS * j - (WS - 2u) * pm;
+                span_sum += s_data[b];
+            } else {
+                span_sum += 1u;
+            }
+        }
+        uint32_t incl = span_sum;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            uint32_t t = __shfl_up_sync(FULL, incl, o);
+            if (lane >= o) incl += t;
+        }
+        const uint32_t total_span = __shfl_sync(FULL, incl, 31);
+        if (total_span != E) {
+            if (lane == 0) atomicOr(a.status, kStatCorrupt);
+            continue;
+        }
+
+        // ---- D4: scatter literals and back-pointers ----
+        bool lane_bad = false;
+        uint32_t q = incl - span_sum;
+        for (uint32_t j = j_lo; j < j_hi; ++j) {
+            uint32_t w = s_fl[j >> 5];
+            bool ism = (w >> (j & 31u)) & 1u;
+            uint32_t pm = s_wp[j >> 5] + __popc(w & ((1u << (j & 31u)) - 1u));
+            uint32_t b = WS * j - (WS - 2u) * pm;
+            if (ism) {
+                uint32_t L = s_data[b], O = s_data[b + 1];
+                if (L == 0 || O == 0 || O > q) {
+                    lane_bad = true;
+                    break;
+                }
+                for (uint32_t k = 0; k < L; ++k) s_src[q + k] = (uint16_t)(q + k - O);
+                q += L;
+            } else {
+                s_src[q] = (uint16_t)(kLit | b);
+                q += 1;
+            }
+        }
+        if (__any_sync(FULL, lane_bad)) {
+            if (lane == 0) atomicOr(a.status, kStatCorrupt);
+            continue;
+        }
+        __syncwarp();
+
+        // ---- D5: pointer jumping ----
+        bool unresolved = true;
+        for (int r = 0; r < kMaxJumpRounds && unresolved; ++r) {
+            bool mine = false;
+            for (uint32_t i = lane; i < E; i += 32) {
+                uint16_t s = s_src[i];
+                if (!(s & kLit)) {
+                    uint16_t s2 = s_src[s];
+                    s_src[i] = s2;
+                    mine |= !(s2 & kLit);
+                }
+            }
+            unresolved = __any_sync(FULL, mine);
+            __syncwarp();
+        }
+        if (unresolved) {
+            if (lane == 0) atomicOr(a.status, kStatCorrupt);
+            continue;
+        }
+
+        // ---- D6: gather and store ----
+        write_chunk(out, take, chunk_out_aligned, lane,
+                    [s_data, s_src](uint32_t j) { return lit_word<WS>(s_data, s_src, j); });
+        __syncwarp();
+    }
+}
+
+__global__ void __launch_bounds__(kDecWarps * 32) decode_kernel(DecodeArgs a) {
+    extern __shared__ __align__(16) uint8_t smem[];
+    const int lane = threadIdx.x & 31;
+    const int warp = threadIdx.x >> 5;
+
+    // ---- D1: parse and validate the header (every warp, lanes 0..7) ----
+    uint32_t hw = 0;
+    const bool hdr_fits = a.in_bytes >= kHeaderBytes;
+    if (lane < 8 && hdr_fits) hw = read_u32(a.in + 4 * lane);
+    uint32_t h[8];
+#pragma unroll
+    for (int k = 0; k < 8; ++k) h[k] = __shfl_sync(FULL, hw, k);
+    Geo g;
+    g.ws = (h[1] >> 16) & 0xFFu;
+    g.cs = h[2];
+    g.C = h[3];
+    g.orig = (uint64_t)h[4] | ((uint64_t)h[5] << 32);
+    g.total = (uint64_t)h[6] | ((uint64_t)h[7] << 32);
+    bool ok = hdr_fits && h[0] == kMagic && (h[1] & 0xFFFFu) == kVersion && (h[1] >> 24) == 0 &&
+              valid_geometry((int)g.ws, (int)g.cs);
+    if (ok) {
+        g.E = g.cs / g.ws;
+        ok = (uint64_t)g.C == (g.orig + g.cs - 1) / g.cs;
+        g.body0 = (uint64_t)kHeaderBytes + (uint64_t)kEntryBytes * g.C;
+        ok = ok && g.total >= g.body0 && g.total <= a.in_bytes;
+    }
+    if (!ok) {
+        if (blockIdx.x == 0 && threadIdx.x == 0) atomicOr(a.status, kStatCorrupt);
+        return;
+    }
+    if (g.orig != a.n_bytes) {
+        if (blockIdx.x == 0 && threadIdx.x == 0) atomicOr(a.status, kStatSizeMismatch);
+        return;
+    }
+    const DecSlot S = dec_slot(g.cs, g.E);
+    const int slots = (int)(kDecSmem / S.total) < kDecWarps ? (int)(kDecSmem / S.total) : kDecWarps;
+    if (warp >= slots) return;
+    uint8_t* slot = smem + (size_t)warp * S.total;
+    if (g.ws == 4)
+        decode_chunks<4>(a, g, slot, lane);
+    else if (g.ws == 2)
+        decode_chunks<2>(a, g, slot, lane);
+    else
+        decode_chunks<1>(a, g, slot, lane);
+}
+
+}  // namespace
+
+cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t stream) {
+    static int configured_dev = -1;
+    static int grid_cache = 0;
+    int dev = 0;
+    cudaError_t err = cudaGetDevice(&dev);
+    if (err != cudaSuccess) return err;
+    if (configured_dev != dev) {
+        err = cudaFuncSetAttribute(decode_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                   (int)kDecSmem);
+        if (err != cudaSuccess) return err;
+        int sms = 0, per_sm = 0;
+        if ((err = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) !=
+            cudaSuccess)
+            return err;
+        if ((err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, decode_kernel,
+                                                                 kDecWarps * 32, kDecSmem)) !=
+            cudaSuccess)
+            return err;
+        grid_cache = sms * (per_sm < 1 ? 1 : per_sm);
+        configured_dev = dev;
+    }
+    // Chunks per stream are bounded by n_bytes / 1024 (the smallest chunk).
+    uint64_t max_chunks = (a.n_bytes + 1023u) / 1024u;
+    uint64_t max_ctas = (max_chunks + kDecWarps - 1) / kDecWarps;
+    uint64_t grid = (uint64_t)grid_cache;
+    if (grid > max_ctas) grid = max_ctas;
+    if (grid < 1) grid = 1;
+    decode_kernel<<<(unsigned)grid, kDecWarps * 32, kDecSmem, stream>>>(a);
+    return cudaGetLastError();
+}
+
+}  // namespace gpulz

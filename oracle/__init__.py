@@ -82,6 +82,10 @@ def _load():
                                                ctypes.c_int, ctypes.c_uint64, ctypes.c_uint64,
                                                u8p, u32p, u32p]
         lib.orc_encode_chunk_range.restype = None
+        u64p = ctypes.POINTER(ctypes.c_uint64)
+        lib.orc_decode_chunk_range.argtypes = [u8p, ctypes.c_uint64, u64p, u8p, ctypes.c_uint64,
+                                               ctypes.c_uint64, ctypes.c_uint64]
+        lib.orc_decode_chunk_range.restype = ctypes.c_int
         _lib = lib
         return lib
 
@@ -216,3 +220,44 @@ def compress_threads(data, word_size: int, chunk_size: int, match_level: int,
     header.view(np.uint64)[3] = total
     table = entries[:2 * chunks].view(np.uint8)
     return np.concatenate([header, table] + body) if chunks else header
+
+
+def decompress_threads(stream, n_bytes: int, threads: int) -> np.ndarray:
+    """The oracle decoder spread over host threads by chunk range.
+
+    Block offsets come from the size table (each block's size follows from its
+    entry); every range is then decoded by the same sequential replay as
+    ``decompress``."""
+    s = _as_bytes(stream)
+    hdr = s[:32]
+    chunk_size = int(hdr[8:12].view(np.uint32)[0])
+    chunks = int(hdr[12:16].view(np.uint32)[0])
+    ent = s[32:32 + 8 * chunks].view(np.uint32).reshape(-1, 2).astype(np.uint64)
+    items, dbytes = ent[:, 0], ent[:, 1]
+    raw = items == 0x80000000
+    zero = (items == 0) & (dbytes == 0)
+    blk = 4 * ((items + 31) // 32) + ((dbytes + 3) & ~np.uint64(3))
+    blk = np.where(raw, np.uint64(chunk_size), np.where(zero, np.uint64(0), blk))
+    offs = np.zeros(max(chunks, 1), np.uint64)
+    if chunks:
+        offs[:chunks] = 32 + 8 * chunks + np.concatenate([[0], np.cumsum(blk)[:-1]]).astype(
+            np.uint64)
+    out = np.zeros(max(n_bytes, 1), np.uint8)
+    lib = _load()
+    threads = max(1, min(threads, max(chunks, 1)))
+    bounds = [chunks * t // threads for t in range(threads + 1)]
+    rcs = [0] * threads
+    optr = offs.ctypes.data_as(ctypes.POINTER(ctypes.c_uint64))
+
+    def run(t):
+        rcs[t] = lib.orc_decode_chunk_range(_u8(s), s.size, optr, _u8(out), n_bytes, bounds[t],
+                                            bounds[t + 1])
+
+    pool = [threading.Thread(target=run, args=(t,)) for t in range(threads)]
+    for th in pool:
+        th.start()
+    for th in pool:
+        th.join()
+    if any(rcs):
+        raise ValueError("oracle decompress failed with code %d" % min(rcs))
+    return out[:n_bytes]

@@ -448,3 +448,41 @@ void orc_encode_chunk_range(const uint8_t* in, uint64_t n_bytes, int word_size, 
     }
     free(chunk);
 }
+
+/* Chunk-range decode used to spread the oracle decoder over host threads:
+ * decodes chunks [c0, c1) of a stream whose per-chunk block offsets (from the
+ * start of the stream) are given in block_off[c]. Returns 0 or ORC_ERR_*. */
+int orc_decode_chunk_range(const uint8_t* in, uint64_t in_len, const uint64_t* block_off,
+                           uint8_t* out, uint64_t n_bytes, uint64_t c0, uint64_t c1) {
+    int ws = 0, cs = 0;
+    uint64_t chunks = 0, orig = 0, total = 0;
+    int rc = orc_parse_header(in, in_len, &ws, &cs, &chunks, &orig, &total);
+    if (rc != 0) return rc;
+    if (orig != n_bytes || total > in_len || c1 > chunks) return ORC_ERR_CORRUPT;
+    int elems = cs / ws;
+    uint8_t* chunk = (uint8_t*)malloc((size_t)cs);
+    for (uint64_t c = c0; c < c1 && rc == 0; ++c) {
+        const uint8_t* e = in + ORC_HEADER_BYTES + ORC_ENTRY_BYTES * c;
+        uint32_t items = get_u32(e), dbytes = get_u32(e + 4);
+        uint64_t pos = block_off[c];
+        if (items == 0 && dbytes == 0) {
+            memset(chunk, 0, (size_t)cs);
+        } else if (items == ORC_RAW_BIT) {
+            if (dbytes != (uint32_t)cs || pos + (uint64_t)cs > total) rc = ORC_ERR_CORRUPT;
+            else memcpy(chunk, in + pos, (size_t)cs);
+        } else if ((items & ORC_RAW_BIT) || items > (uint32_t)elems || dbytes > (uint32_t)cs) {
+            rc = ORC_ERR_CORRUPT;
+        } else {
+            uint64_t blk = 4u * ((items + 31u) / 32u) + ((dbytes + 3u) & ~3u);
+            if (pos + blk > total) rc = ORC_ERR_CORRUPT;
+            else rc = decode_items(in + pos, items, dbytes, ws, cs, chunk);
+        }
+        if (rc != 0) break;
+        uint64_t begin = c * (uint64_t)cs;
+        uint64_t take = n_bytes - begin;
+        if (take > (uint64_t)cs) take = (uint64_t)cs;
+        memcpy(out + begin, chunk, (size_t)take);
+    }
+    free(chunk);
+    return rc;
+}

@@ -44,6 +44,9 @@ void orc_encode_chunk_range(const uint8_t* in, uint64_t n_bytes, int word_size, 
                             int match_level, uint64_t c0, uint64_t c1, uint8_t* out_blocks,
                             uint32_t* block_bytes, uint32_t* entries);
 
+int orc_decode_chunk_range(const uint8_t* in, uint64_t in_len, const uint64_t* block_off,
+                           uint8_t* out, uint64_t n_bytes, uint64_t c0, uint64_t c1);
+
 #ifdef __cplusplus
 }
 #endif

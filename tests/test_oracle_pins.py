@@ -281,6 +281,10 @@ def test_threaded_oracle_matches_sequential(orc):
         a = orc.compress(x, 4, 2048, lvl)
         b = orc.compress_threads(x, 4, 2048, lvl, threads=4)
         assert np.array_equal(a, b)
+        assert np.array_equal(orc.decompress_threads(a, x.size, threads=3), x)
+    z = np.zeros(3 * 1024 + 5, np.uint8)
+    s = orc.compress(z, 1, 1024, 1)
+    assert np.array_equal(orc.decompress_threads(s, z.size, threads=2), z)
 
 
 # ----------------------------------------------------------------------------
