@@ -53,6 +53,10 @@ __device__ __forceinline__ DecSlot dec_slot(uint32_t cs, uint32_t E) {
     return s;
 }
 
+__device__ __forceinline__ uint32_t read_u32(const uint8_t* p) {
+    return *reinterpret_cast<const uint32_t*>(p);
+}
+
 // Block size of a size-table entry; 0xFFFFFFFF if the entry is invalid.
 __device__ __forceinline__ uint32_t entry_block(uint32_t items, uint32_t dbytes, const Geo& g) {
     if (items == 0 && dbytes == 0) return 0;
@@ -62,36 +66,51 @@ __device__ __forceinline__ uint32_t entry_block(uint32_t items, uint32_t dbytes,
     return blk < g.cs ? blk : 0xFFFFFFFFu;
 }
 
-__device__ __forceinline__ uint32_t read_u32(const uint8_t* p) {
-    return *reinterpret_cast<const uint32_t*>(p);
-}
+
+// Exclusive prefix of block bytes over chunks [0, c). Every block size is in
+// the size table, so nothing is awaited: predecessors that have published an
+// inclusive offset end the walk, the others contribute their table entry.
+// kLookBackPerLane descriptors per lane and step keep the loads overlapped.
+constexpr int kLookBackPerLane = 8;
+constexpr int kLookBackWidth = 32 * kLookBackPerLane;
 
 __device__ uint64_t lookback_decode(const DecodeArgs& a, const Geo& g, uint32_t c, uint64_t blk,
                                     int lane) {
     uint64_t prefix = 0;
     int64_t base = (int64_t)c - 1;
     while (base >= 0) {
-        int64_t idx = base - lane;
-        bool incl = true;
-        uint64_t val = 0;
-        if (idx >= 0) {
-            uint64_t d = ld_relaxed_u64(&a.desc[idx]);
-            incl = desc_epoch(d) == a.epoch && desc_kind(d) == kDescInclusive;
-            val = desc_value(d);
+        uint64_t d[kLookBackPerLane];
+#pragma unroll
+        for (int k = 0; k < kLookBackPerLane; ++k) {
+            int64_t idx = base - (k * 32 + lane);
+            d[k] = idx >= 0 ? ld_relaxed_u64(&a.desc[idx]) : make_desc(a.epoch, kDescInclusive, 0);
         }
-        uint32_t m = __ballot_sync(FULL, incl);
-        int f = m ? __ffs(m) - 1 : 32;
+        uint32_t my_min = 0xFFFFFFFFu;
+#pragma unroll
+        for (int k = kLookBackPerLane - 1; k >= 0; --k) {
+            if (desc_epoch(d[k]) == a.epoch && desc_kind(d[k]) == kDescInclusive)
+                my_min = (uint32_t)(k * 32 + lane);
+        }
+        const uint32_t dmin = __reduce_min_sync(FULL, my_min);
+        const uint32_t lim = dmin == 0xFFFFFFFFu ? (uint32_t)kLookBackWidth : dmin + 1u;
         uint64_t v = 0;
-        if (lane < f && idx >= 0) {
-            const uint8_t* e = a.in + kHeaderBytes + (uint64_t)kEntryBytes * (uint64_t)idx;
-            uint32_t b = entry_block(read_u32(e), read_u32(e + 4), g);
-            v = b == 0xFFFFFFFFu ? 0 : b;
-        } else if (lane == f) {
-            v = val;
+#pragma unroll
+        for (int k = 0; k < kLookBackPerLane; ++k) {
+            const uint32_t dist = (uint32_t)(k * 32 + lane);
+            const int64_t idx = base - (int64_t)dist;
+            if (dist < lim) {
+                if (dist == dmin) {
+                    v += desc_value(d[k]);
+                } else if (idx >= 0) {
+                    const uint8_t* e = a.in + kHeaderBytes + (uint64_t)kEntryBytes * (uint64_t)idx;
+                    const uint32_t b = entry_block(read_u32(e), read_u32(e + 4), g);
+                    v += b == 0xFFFFFFFFu ? 0u : b;
+                }
+            }
         }
         prefix += warp_sum_u64(v);
-        if (f < 32) break;
-        base -= 32;
+        if (dmin != 0xFFFFFFFFu) break;
+        base -= kLookBackWidth;
     }
     if (lane == 0) st_relaxed_u64(&a.desc[c], make_desc(a.epoch, kDescInclusive, prefix + blk));
     return prefix;

@@ -194,43 +194,63 @@ __device__ __forceinline__ void publish_aggregate(const EncodeArgs& a, uint32_t 
                    make_desc(a.epoch, c == 0 ? kDescInclusive : kDescAggregate, aggregate));
 }
 
-// Exclusive prefix of block bytes over chunks [0, c) by decoupled look-back
-// (warp-wide: 32 predecessors per step). The aggregate of chunk c must have
-// been published. Waits are bounded by kWaitLimitNs of device time.
+// Exclusive prefix of block bytes over chunks [0, c) by decoupled look-back.
+// The warp inspects kLookBackWidth predecessors per step (each lane loads
+// kLookBackPerLane descriptors, so the loads overlap): it sums aggregates back
+// to the nearest inclusive prefix. The aggregate of chunk c must already be
+// published. Waits are bounded by kWaitLimitNs of device time.
+constexpr int kLookBackPerLane = 8;
+constexpr int kLookBackWidth = 32 * kLookBackPerLane;
+
 __device__ uint64_t lookback_encode(const EncodeArgs& a, uint32_t c, uint64_t aggregate, int lane,
                                     bool* timed_out) {
     *timed_out = false;
     if (c == 0) return 0;
-    uint64_t* desc = a.desc;
+    const uint64_t* desc = a.desc;
     uint64_t prefix = 0;
     int64_t base = (int64_t)c - 1;
     uint64_t t0 = 0;
     for (;;) {
-        int64_t idx = base - lane;
-        uint64_t d = idx >= 0 ? ld_relaxed_u64(&desc[idx]) : make_desc(a.epoch, kDescInclusive, 0);
-        bool valid = desc_epoch(d) == a.epoch && desc_kind(d) != 0;
-        bool incl = valid && desc_kind(d) == kDescInclusive;
-        uint32_t incl_mask = __ballot_sync(FULL, incl);
-        uint32_t bad_mask = __ballot_sync(FULL, !valid);
-        int f = incl_mask ? __ffs(incl_mask) - 1 : 32;
-        uint32_t need = f >= 31 ? FULL : ((2u << f) - 1u);
-        if (bad_mask & need) {
+        uint64_t d[kLookBackPerLane];
+#pragma unroll
+        for (int k = 0; k < kLookBackPerLane; ++k) {
+            int64_t idx = base - (k * 32 + lane);
+            d[k] = idx >= 0 ? ld_relaxed_u64(&desc[idx]) : make_desc(a.epoch, kDescInclusive, 0);
+        }
+        uint32_t my_min = 0xFFFFFFFFu;
+#pragma unroll
+        for (int k = kLookBackPerLane - 1; k >= 0; --k) {
+            bool incl = desc_epoch(d[k]) == a.epoch && desc_kind(d[k]) == kDescInclusive;
+            if (incl) my_min = (uint32_t)(k * 32 + lane);
+        }
+        const uint32_t dmin = __reduce_min_sync(FULL, my_min);
+        const uint32_t lim = dmin == 0xFFFFFFFFu ? (uint32_t)kLookBackWidth : dmin + 1u;
+        bool bad = false;
+        uint64_t v = 0;
+#pragma unroll
+        for (int k = 0; k < kLookBackPerLane; ++k) {
+            if ((uint32_t)(k * 32 + lane) < lim) {
+                bool valid = desc_epoch(d[k]) == a.epoch && desc_kind(d[k]) != 0;
+                bad |= !valid;
+                v += desc_value(d[k]);
+            }
+        }
+        if (__any_sync(FULL, bad)) {
             uint64_t now = globaltimer_ns();
             if (t0 == 0) t0 = now;
             if (now - t0 > kWaitLimitNs) {
                 *timed_out = true;
                 break;
             }
-            __nanosleep(64);
+            __nanosleep(32);
             continue;
         }
-        uint64_t v = (lane <= f) ? desc_value(d) : 0ull;
         prefix += warp_sum_u64(v);
-        if (f < 32) break;
-        base -= 32;
+        if (dmin != 0xFFFFFFFFu) break;
+        base -= kLookBackWidth;
     }
     if (lane == 0)
-        st_relaxed_u64(&desc[c], make_desc(a.epoch, kDescInclusive, prefix + aggregate));
+        st_relaxed_u64(&a.desc[c], make_desc(a.epoch, kDescInclusive, prefix + aggregate));
     return prefix;
 }
 
@@ -239,17 +259,16 @@ __device__ void store_u32_capped(uint8_t* out, uint64_t off, uint32_t v, uint64_
 }
 
 __device__ void write_header(const EncodeArgs& a, uint32_t ws, uint64_t total) {
-    if (a.capacity >= kHeaderBytes) {
-        uint32_t* h = reinterpret_cast<uint32_t*>(a.out);
-        h[0] = kMagic;
-        h[1] = kVersion | (ws << 16);  // u16 version, u8 word_size, u8 reserved
-        h[2] = a.chunk_size;
-        h[3] = a.n_chunks;
-        h[4] = (uint32_t)a.n_bytes;
-        h[5] = (uint32_t)(a.n_bytes >> 32);
-        h[6] = (uint32_t)total;
-        h[7] = (uint32_t)(total >> 32);
-    }
+    const uint32_t h[8] = {kMagic,
+                           kVersion | (ws << 16),  // u16 version, u8 word_size, u8 reserved
+                           a.chunk_size,
+                           a.n_chunks,
+                           (uint32_t)a.n_bytes,
+                           (uint32_t)(a.n_bytes >> 32),
+                           (uint32_t)total,
+                           (uint32_t)(total >> 32)};
+#pragma unroll
+    for (int k = 0; k < 8; ++k) store_u32_capped(a.out, 4ull * k, h[k], a.capacity);
     *a.out_bytes = (unsigned long long)total;
     if (total > a.capacity) atomicOr(a.status, kStatCapacity);
 }
