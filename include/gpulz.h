@@ -123,6 +123,35 @@ gpulz_status gpulz_stream_info(const void* h_header, size_t h_len, size_t* orig_
  * the last call (GPULZ_OK if none) and clear it. */
 gpulz_status gpulz_device_status(cudaStream_t stream);
 
+/*
+ * gpulz_compress_noalloc -- gpulz_compress for callers that cannot allocate.
+ * (No counterpart in the paper: the GPULZ pages have no such entry point.)
+ *
+ * Some callers cannot let a library call cudaMalloc: code running while a
+ * framework's caching allocator already holds the device memory, code on a
+ * latency-critical path that cannot take cudaMalloc's implicit device-wide
+ * synchronisation, and plug-ins whose host forbids allocations it does not
+ * make. This entry point never allocates and calls no allocating routine. Its
+ * scratch (look-back descriptors, ticket counter, status word) is one fixed
+ * device array of about 512 KiB inside the library, which every GPU that
+ * loads the library holds until the process exits.
+ *
+ * Arguments, output and stream format are exactly those of gpulz_compress.
+ * Limit: at most 65536 chunks per call (256 MiB of input at chunk_size 4096,
+ * 128 MiB at 2048, 64 MiB at 1024); larger inputs return
+ * GPULZ_ERR_INVALID_ARG and launch nothing.
+ * Set-up: the first call on a device looks up the array's device address with
+ * that device current; make that first call before any stream capture.
+ * Sharing: all calls on a device share the one array and each call clears it
+ * on its stream first, so calls that overlap on the GPU (other streams, other
+ * host threads) race and must not be issued. A device-side wait that gives up
+ * sets *d_out_bytes to SIZE_MAX; capacity overflow shows as
+ * *d_out_bytes > capacity. gpulz_device_status() does not see this path.
+ */
+gpulz_status gpulz_compress_noalloc(const void* d_in, size_t n_bytes, int word_size,
+                                    int chunk_size, int match_level, void* d_out,
+                                    size_t capacity, size_t* d_out_bytes, cudaStream_t stream);
+
 /* Static, human-readable name of a status code. */
 const char* gpulz_status_string(gpulz_status status);
 

@@ -17,7 +17,7 @@ import os
 __all__ = [
     "GPULZ_OK", "GPULZ_ERR_INVALID_ARG", "GPULZ_ERR_CAPACITY", "GPULZ_ERR_CORRUPT",
     "GPULZ_ERR_TIMEOUT", "GPULZ_ERR_CUDA", "GPULZ_ERR_SIZE_MISMATCH", "GpulzError",
-    "library_path", "load", "build", "gpulz_compress", "gpulz_decompress",
+    "library_path", "load", "build", "gpulz_compress", "gpulz_compress_noalloc", "gpulz_decompress",
     "gpulz_decompress_bounded", "gpulz_compress_bound", "gpulz_stream_info",
     "gpulz_device_status", "gpulz_status_string", "compress", "decompress",
 ]
@@ -62,6 +62,8 @@ def load():
     vp, sz, i32 = ctypes.c_void_p, ctypes.c_size_t, ctypes.c_int
     lib.gpulz_compress.argtypes = [vp, sz, i32, i32, i32, vp, sz, vp, vp]
     lib.gpulz_compress.restype = i32
+    lib.gpulz_compress_noalloc.argtypes = [vp, sz, i32, i32, i32, vp, sz, vp, vp]
+    lib.gpulz_compress_noalloc.restype = i32
     lib.gpulz_decompress.argtypes = [vp, vp, sz, vp]
     lib.gpulz_decompress.restype = i32
     lib.gpulz_decompress_bounded.argtypes = [vp, sz, vp, sz, vp]
@@ -108,6 +110,14 @@ def gpulz_compress(d_in, n_bytes, word_size, chunk_size, match_level, d_out, cap
                    d_out_bytes, stream=None) -> int:
     return load().gpulz_compress(_ptr(d_in), n_bytes, word_size, chunk_size, match_level,
                                  _ptr(d_out), capacity, _ptr(d_out_bytes), _stream(stream))
+
+
+def gpulz_compress_noalloc(d_in, n_bytes, word_size, chunk_size, match_level, d_out, capacity,
+                           d_out_bytes, stream=None) -> int:
+    """gpulz_compress for callers that cannot allocate (fixed in-library scratch)."""
+    return load().gpulz_compress_noalloc(_ptr(d_in), n_bytes, word_size, chunk_size, match_level,
+                                         _ptr(d_out), capacity, _ptr(d_out_bytes),
+                                         _stream(stream))
 
 
 def gpulz_decompress(d_in, d_out, n_bytes, stream=None) -> int:

@@ -1,0 +1,97 @@
+// gpulz_compress_noalloc: the encode path with its scratch in a fixed,
+// file-scope device array instead of memory the library allocates.
+//
+// Some callers cannot let a library call cudaMalloc: code that runs while a
+// framework's caching allocator has already reserved the device memory, code
+// on a latency-critical path where cudaMalloc's implicit device-wide
+// synchronisation is not acceptable, and plug-ins whose host forbids
+// allocations behind its back. This entry point serves them: it allocates
+// nothing, ever. Its look-back descriptors, ticket counter and status word live
+// in g_noalloc_scratch below, which every GPU that loads the library holds
+// until the process exits.
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include <mutex>
+
+#include "../../include/gpulz.h"
+#include "gpulz_internal.cuh"
+
+namespace {
+
+using namespace gpulz;
+
+// Largest input the fixed scratch can serve: one 8-byte descriptor per chunk.
+constexpr uint64_t kNoAllocMaxChunks = 65536;
+constexpr size_t kNoAllocHead = 256;  // u32 status at 0, u32 ticket at 4
+constexpr size_t kNoAllocBytes = kNoAllocHead + sizeof(uint64_t) * kNoAllocMaxChunks;
+
+static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocBytes];
+
+constexpr int kMaxDevices = 64;
+std::mutex g_mu;
+uint8_t* g_scratch_dev[kMaxDevices] = {};
+
+// Device address of g_noalloc_scratch on the current device, looked up once
+// per device with that device current.
+cudaError_t scratch_address(uint8_t** out) {
+    int dev = 0;
+    cudaError_t err = cudaGetDevice(&dev);
+    if (err != cudaSuccess) return err;
+    if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+    std::lock_guard<std::mutex> lock(g_mu);
+    if (g_scratch_dev[dev] == nullptr) {
+        void* p = nullptr;
+        err = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+        if (err != cudaSuccess) return err;
+        g_scratch_dev[dev] = static_cast<uint8_t*>(p);
+    }
+    *out = g_scratch_dev[dev];
+    return cudaSuccess;
+}
+
+// A bounded look-back wait that gave up is reported through the length:
+// *d_out_bytes = SIZE_MAX.
+__global__ void noalloc_report(const uint32_t* status, unsigned long long* out_bytes) {
+    if (threadIdx.x == 0 && (*status & kStatTimeout)) *out_bytes = ~0ull;
+}
+
+}  // namespace
+
+extern "C" gpulz_status gpulz_compress_noalloc(const void* d_in, size_t n_bytes, int word_size,
+                                               int chunk_size, int match_level, void* d_out,
+                                               size_t capacity, size_t* d_out_bytes,
+                                               cudaStream_t stream) {
+    if (!valid_geometry(word_size, chunk_size)) return GPULZ_ERR_INVALID_ARG;
+    if (match_level != 0 && match_level != 1) return GPULZ_ERR_INVALID_ARG;
+    if ((n_bytes > 0 && d_in == nullptr) || d_out == nullptr || d_out_bytes == nullptr)
+        return GPULZ_ERR_INVALID_ARG;
+    if ((reinterpret_cast<uintptr_t>(d_out) & 3u) || (reinterpret_cast<uintptr_t>(d_out_bytes) & 7u))
+        return GPULZ_ERR_INVALID_ARG;
+    const uint64_t chunks = ((uint64_t)n_bytes + chunk_size - 1) / (uint64_t)chunk_size;
+    if (chunks > kNoAllocMaxChunks) return GPULZ_ERR_INVALID_ARG;
+    uint8_t* base = nullptr;
+    if (scratch_address(&base) != cudaSuccess) return GPULZ_ERR_CUDA;
+    // The array keeps the previous call's contents: clear the status, the
+    // ticket and this call's descriptors, in stream order.
+    if (cudaMemsetAsync(base, 0, kNoAllocHead + sizeof(uint64_t) * chunks, stream) != cudaSuccess)
+        return GPULZ_ERR_CUDA;
+    EncodeArgs a;
+    a.in = static_cast<const uint8_t*>(d_in);
+    a.n_bytes = n_bytes;
+    a.out = static_cast<uint8_t*>(d_out);
+    a.capacity = capacity;
+    a.out_bytes = reinterpret_cast<unsigned long long*>(d_out_bytes);
+    a.desc = reinterpret_cast<uint64_t*>(base + kNoAllocHead);
+    a.ticket = reinterpret_cast<uint32_t*>(base + 4);
+    a.status = reinterpret_cast<uint32_t*>(base);
+    a.epoch = 1;
+    a.chunk_size = (uint32_t)chunk_size;
+    a.elems = (uint32_t)(chunk_size / word_size);
+    a.n_chunks = (uint32_t)chunks;
+    a.hash_bits = log2_exact(2u * a.elems);
+    if (launch_encode(a, word_size, match_level, stream) != cudaSuccess) return GPULZ_ERR_CUDA;
+    noalloc_report<<<1, 32, 0, stream>>>(a.status, a.out_bytes);
+    if (cudaGetLastError() != cudaSuccess) return GPULZ_ERR_CUDA;
+    return GPULZ_OK;
+}
