@@ -15,27 +15,32 @@ namespace {
 
 using namespace gpulz;
 
-// Scratch of one (device, stream): status word, one ticket counter per epoch,
-// look-back descriptors. A call takes the next epoch; descriptors and tickets
-// of other epochs never match, so nothing is cleared between calls. When the
-// 16-bit epoch wraps, the whole area is cleared once on the stream.
+// Scratch of one (device, stream): status word, two ticket counters per
+// epoch, tile descriptors, one word per chunk (block sizes or offsets) and,
+// for the two-pass encode, one chunk_size slot per chunk. A call takes the
+// next epoch; descriptors and tickets of other epochs never match, so nothing
+// is cleared between calls. When the 16-bit epoch wraps, the whole area is
+// cleared once on the stream.
 struct Scratch {
     int device;
     cudaStream_t stream;
     uint8_t* base;
-    uint64_t desc_capacity;  // chunks
-    uint32_t epoch;          // last epoch used
+    uint64_t cap_chunks;
+    uint64_t slot_bytes;
+    uint32_t epoch;  // last epoch used
 };
 
 std::mutex g_mu;
 std::vector<Scratch*> g_scratch;
 
-size_t scratch_bytes(uint64_t chunks) { return kDescOffset + sizeof(uint64_t) * chunks; }
+size_t scratch_bytes(uint64_t cap_chunks, uint64_t slot_bytes) {
+    return kStateOffset + scratch_regions(cap_chunks, slot_bytes).end;
+}
 
 // Returns the scratch for (current device, stream) with room for `chunks`
-// descriptors and advances its epoch; *epoch_out receives the epoch to use.
-cudaError_t acquire_scratch(cudaStream_t stream, uint64_t chunks, Scratch** out,
-                            uint32_t* epoch_out) {
+// per-chunk words and `slot_bytes` of slots, and advances its epoch.
+cudaError_t acquire_scratch(cudaStream_t stream, uint64_t chunks, uint64_t slot_bytes,
+                            Scratch** out, uint32_t* epoch_out) {
     int dev = 0;
     cudaError_t err = cudaGetDevice(&dev);
     if (err != cudaSuccess) return err;
@@ -44,14 +49,18 @@ cudaError_t acquire_scratch(cudaStream_t stream, uint64_t chunks, Scratch** out,
     for (Scratch* t : g_scratch)
         if (t->device == dev && t->stream == stream) s = t;
     if (s == nullptr) {
-        s = new Scratch{dev, stream, nullptr, 0, 0};
+        s = new Scratch{dev, stream, nullptr, 0, 0, 0};
         g_scratch.push_back(s);
     }
-    if (s->base == nullptr || s->desc_capacity < chunks) {
-        uint64_t cap = chunks < 4096 ? 4096 : chunks;
+    if (s->base == nullptr || s->cap_chunks < chunks || s->slot_bytes < slot_bytes) {
+        const uint64_t cap = chunks < 4096 ? 4096 : (chunks > s->cap_chunks ? chunks : s->cap_chunks);
+        const uint64_t sb = slot_bytes > s->slot_bytes ? slot_bytes : s->slot_bytes;
         void* p = nullptr;
-        if ((err = cudaMallocAsync(&p, scratch_bytes(cap), stream)) != cudaSuccess) return err;
-        if ((err = cudaMemsetAsync(p, 0, scratch_bytes(cap), stream)) != cudaSuccess) return err;
+        if ((err = cudaMallocAsync(&p, scratch_bytes(cap, sb), stream)) != cudaSuccess) return err;
+        // slots need no clearing: every byte read from a slot was written by the same call
+        if ((err = cudaMemsetAsync(p, 0, kStateOffset + scratch_regions(cap, sb).slots, stream)) !=
+            cudaSuccess)
+            return err;
         if (s->base != nullptr) {
             // keep recorded errors; earlier work on this stream still owns the old area,
             // so it is released in stream order
@@ -62,15 +71,17 @@ cudaError_t acquire_scratch(cudaStream_t stream, uint64_t chunks, Scratch** out,
             s->base = nullptr;
         }
         s->base = static_cast<uint8_t*>(p);
-        s->desc_capacity = cap;
+        s->cap_chunks = cap;
+        s->slot_bytes = sb;
         s->epoch = 0;
     }
     s->epoch += 1;
     if (s->epoch >= kEpochs) {
         // clear tickets and descriptors (keep the status word)
         if ((err = cudaMemsetAsync(s->base + kTicketOffset, 0,
-                                   scratch_bytes(s->desc_capacity) - kTicketOffset, stream)) !=
-            cudaSuccess)
+                                   kStateOffset - kTicketOffset +
+                                       scratch_regions(s->cap_chunks, s->slot_bytes).slots,
+                                   stream)) != cudaSuccess)
             return err;
         s->epoch = 1;
     }
@@ -114,22 +125,32 @@ gpulz_status gpulz_compress(const void* d_in, size_t n_bytes, int word_size, int
     if (chunks > 0xFFFFFFFFull) return GPULZ_ERR_INVALID_ARG;
     Scratch* s = nullptr;
     uint32_t epoch = 0;
-    if (acquire_scratch(stream, chunks, &s, &epoch) != cudaSuccess) return GPULZ_ERR_CUDA;
+    if (acquire_scratch(stream, chunks, chunks * (uint64_t)chunk_size, &s, &epoch) != cudaSuccess)
+        return GPULZ_ERR_CUDA;
+    const ScratchRegions r = scratch_regions(s->cap_chunks, s->slot_bytes);
+    uint8_t* st = s->base + kStateOffset;
+    uint32_t* tickets = reinterpret_cast<uint32_t*>(s->base + kTicketOffset);
     EncodeArgs a;
     a.in = static_cast<const uint8_t*>(d_in);
     a.n_bytes = n_bytes;
     a.out = static_cast<uint8_t*>(d_out);
     a.capacity = capacity;
     a.out_bytes = reinterpret_cast<unsigned long long*>(d_out_bytes);
-    a.desc = reinterpret_cast<uint64_t*>(s->base + kDescOffset);
-    a.ticket = reinterpret_cast<uint32_t*>(s->base + kTicketOffset) + epoch;
+    a.desc = nullptr;
+    a.slots = st + r.slots;
+    a.sizes = reinterpret_cast<uint32_t*>(st + r.sizes);
+    a.offsets = reinterpret_cast<uint64_t*>(st + r.offsets);
+    a.tdesc = reinterpret_cast<uint64_t*>(st + r.tdesc);
+    a.ticket = tickets + 2 * epoch;
+    a.ticket2 = tickets + 2 * epoch + 1;
     a.status = reinterpret_cast<uint32_t*>(s->base);
     a.epoch = epoch;
     a.chunk_size = (uint32_t)chunk_size;
     a.elems = (uint32_t)(chunk_size / word_size);
     a.n_chunks = (uint32_t)chunks;
     a.hash_bits = log2_exact(2u * a.elems);
-    if (launch_encode(a, word_size, match_level, stream) != cudaSuccess) return GPULZ_ERR_CUDA;
+    if (launch_encode(a, word_size, match_level, false, stream) != cudaSuccess)
+        return GPULZ_ERR_CUDA;
     return GPULZ_OK;
 }
 
@@ -140,14 +161,19 @@ gpulz_status gpulz_decompress_bounded(const void* d_in, size_t in_bytes, void* d
     const uint64_t max_chunks = ((uint64_t)n_bytes + 1023u) / 1024u;
     Scratch* s = nullptr;
     uint32_t epoch = 0;
-    if (acquire_scratch(stream, max_chunks, &s, &epoch) != cudaSuccess) return GPULZ_ERR_CUDA;
+    if (acquire_scratch(stream, max_chunks, 0, &s, &epoch) != cudaSuccess) return GPULZ_ERR_CUDA;
+    const ScratchRegions r = scratch_regions(s->cap_chunks, s->slot_bytes);
+    uint8_t* st = s->base + kStateOffset;
+    uint32_t* tickets = reinterpret_cast<uint32_t*>(s->base + kTicketOffset);
     DecodeArgs a;
     a.in = static_cast<const uint8_t*>(d_in);
     a.in_bytes = in_bytes;
     a.out = static_cast<uint8_t*>(d_out);
     a.n_bytes = n_bytes;
-    a.desc = reinterpret_cast<uint64_t*>(s->base + kDescOffset);
-    a.ticket = reinterpret_cast<uint32_t*>(s->base + kTicketOffset) + epoch;
+    a.offsets = reinterpret_cast<uint64_t*>(st + r.offsets);
+    a.tdesc = reinterpret_cast<uint64_t*>(st + r.tdesc);
+    a.ticket = tickets + 2 * epoch;
+    a.ticket2 = tickets + 2 * epoch + 1;
     a.status = reinterpret_cast<uint32_t*>(s->base);
     a.epoch = epoch;
     if (launch_decode(a, stream) != cudaSuccess) return GPULZ_ERR_CUDA;

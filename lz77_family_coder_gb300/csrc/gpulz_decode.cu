@@ -67,55 +67,6 @@ __device__ __forceinline__ uint32_t entry_block(uint32_t items, uint32_t dbytes,
 }
 
 
-// Exclusive prefix of block bytes over chunks [0, c). Every block size is in
-// the size table, so nothing is awaited: predecessors that have published an
-// inclusive offset end the walk, the others contribute their table entry.
-// kLookBackPerLane descriptors per lane and step keep the loads overlapped.
-constexpr int kLookBackPerLane = 8;
-constexpr int kLookBackWidth = 32 * kLookBackPerLane;
-
-__device__ uint64_t lookback_decode(const DecodeArgs& a, const Geo& g, uint32_t c, uint64_t blk,
-                                    int lane) {
-    uint64_t prefix = 0;
-    int64_t base = (int64_t)c - 1;
-    while (base >= 0) {
-        uint64_t d[kLookBackPerLane];
-#pragma unroll
-        for (int k = 0; k < kLookBackPerLane; ++k) {
-            int64_t idx = base - (k * 32 + lane);
-            d[k] = idx >= 0 ? ld_relaxed_u64(&a.desc[idx]) : make_desc(a.epoch, kDescInclusive, 0);
-        }
-        uint32_t my_min = 0xFFFFFFFFu;
-#pragma unroll
-        for (int k = kLookBackPerLane - 1; k >= 0; --k) {
-            if (desc_epoch(d[k]) == a.epoch && desc_kind(d[k]) == kDescInclusive)
-                my_min = (uint32_t)(k * 32 + lane);
-        }
-        const uint32_t dmin = __reduce_min_sync(FULL, my_min);
-        const uint32_t lim = dmin == 0xFFFFFFFFu ? (uint32_t)kLookBackWidth : dmin + 1u;
-        uint64_t v = 0;
-#pragma unroll
-        for (int k = 0; k < kLookBackPerLane; ++k) {
-            const uint32_t dist = (uint32_t)(k * 32 + lane);
-            const int64_t idx = base - (int64_t)dist;
-            if (dist < lim) {
-                if (dist == dmin) {
-                    v += desc_value(d[k]);
-                } else if (idx >= 0) {
-                    const uint8_t* e = a.in + kHeaderBytes + (uint64_t)kEntryBytes * (uint64_t)idx;
-                    const uint32_t b = entry_block(read_u32(e), read_u32(e + 4), g);
-                    v += b == 0xFFFFFFFFu ? 0u : b;
-                }
-            }
-        }
-        prefix += warp_sum_u64(v);
-        if (dmin != 0xFFFFFFFFu) break;
-        base -= kLookBackWidth;
-    }
-    if (lane == 0) st_relaxed_u64(&a.desc[c], make_desc(a.epoch, kDescInclusive, prefix + blk));
-    return prefix;
-}
-
 // Output a chunk as 32-bit words: word j covers chunk bytes [4j, 4j+4).
 template <typename F>
 __device__ __forceinline__ void write_chunk(uint8_t* out, uint32_t take, bool out_aligned, int lane,
@@ -167,7 +118,7 @@ __device__ void decode_chunks(const DecodeArgs& a, const Geo& g, uint8_t* slot_b
     const bool out_aligned = (reinterpret_cast<uintptr_t>(a.out) & 3u) == 0;
     for (;;) {
         uint32_t c = 0;
-        if (lane == 0) c = atomicAdd(a.ticket, 1u);
+        if (lane == 0) c = atomicAdd(a.ticket2, 1u);
         c = __shfl_sync(FULL, c, 0);
         if (c >= g.C) break;
 
@@ -175,10 +126,8 @@ __device__ void decode_chunks(const DecodeArgs& a, const Geo& g, uint8_t* slot_b
         const uint32_t items = read_u32(e), dbytes = read_u32(e + 4);
         uint32_t blk = entry_block(items, dbytes, g);
         bool bad = blk == 0xFFFFFFFFu;
-        const uint64_t prefix = lookback_decode(a, g, c, bad ? 0 : blk, lane);
-        const uint64_t src_off = g.body0 + prefix;
-        if (!bad && src_off + blk > g.total) bad = true;
-        if (c == g.C - 1 && !bad && src_off + blk != g.total) bad = true;
+        const uint64_t src_off = a.offsets[c];
+        if (!bad && (src_off < g.body0 || src_off + blk > g.total)) bad = true;
 
         const uint64_t begin = (uint64_t)c * CS;
         const uint64_t avail = g.orig - begin;
@@ -317,19 +266,17 @@ __device__ void decode_chunks(const DecodeArgs& a, const Geo& g, uint8_t* slot_b
     }
 }
 
-__global__ void __launch_bounds__(kDecWarps * 32) decode_kernel(DecodeArgs a) {
-    extern __shared__ __align__(16) uint8_t smem[];
+// Parse and validate the stream header (every warp, lanes 0..7 load it).
+// Records the reason in the status word (CTA 0, thread 0) and returns false
+// when decoding must not proceed.
+__device__ bool parse_header(const DecodeArgs& a, Geo& g) {
     const int lane = threadIdx.x & 31;
-    const int warp = threadIdx.x >> 5;
-
-    // ---- D1: parse and validate the header (every warp, lanes 0..7) ----
     uint32_t hw = 0;
     const bool hdr_fits = a.in_bytes >= kHeaderBytes;
     if (lane < 8 && hdr_fits) hw = read_u32(a.in + 4 * lane);
     uint32_t h[8];
 #pragma unroll
     for (int k = 0; k < 8; ++k) h[k] = __shfl_sync(FULL, hw, k);
-    Geo g;
     g.ws = (h[1] >> 16) & 0xFFu;
     g.cs = h[2];
     g.C = h[3];
@@ -345,12 +292,48 @@ __global__ void __launch_bounds__(kDecWarps * 32) decode_kernel(DecodeArgs a) {
     }
     if (!ok) {
         if (blockIdx.x == 0 && threadIdx.x == 0) atomicOr(a.status, kStatCorrupt);
-        return;
+        return false;
     }
     if (g.orig != a.n_bytes) {
         if (blockIdx.x == 0 && threadIdx.x == 0) atomicOr(a.status, kStatSizeMismatch);
-        return;
+        return false;
     }
+    return true;
+}
+
+// ---- D1: stream offset of every chunk's block (scan of the size table) ----
+__global__ void __launch_bounds__(kScanThreads) offsets_kernel(DecodeArgs a) {
+    __shared__ TileSmem sm;
+    Geo g;
+    if (!parse_header(a, g)) return;
+    const int tid = threadIdx.x;
+    const uint32_t n_tiles = (g.C + kTile - 1) / kTile;
+    for (;;) {
+        if (tid == 0) sm.tile = atomicAdd(a.ticket, 1u);
+        __syncthreads();
+        const uint32_t t = sm.tile;
+        if (t >= n_tiles) break;
+        const uint64_t prefix = tile_scan(sm, t, g.C, a.tdesc, a.epoch, a.status, [&](uint32_t c) {
+            const uint8_t* e = a.in + kHeaderBytes + (uint64_t)kEntryBytes * c;
+            const uint32_t b = entry_block(read_u32(e), read_u32(e + 4), g);
+            return b == 0xFFFFFFFFu ? 0u : b;
+        });
+        const uint32_t c0 = t * kTile;
+        for (uint32_t j = (uint32_t)tid; j < kTile && c0 + j < g.C; j += kScanThreads)
+            a.offsets[c0 + j] = g.body0 + prefix + sm.off[j];
+        if (t == n_tiles - 1 && tid == 0 && g.body0 + prefix + sm.total != g.total)
+            atomicOr(a.status, kStatCorrupt);
+        __syncthreads();
+    }
+}
+
+// ---- D2..D6: decode, one chunk per warp ----
+__global__ void __launch_bounds__(kDecWarps * 32) decode_kernel(DecodeArgs a) {
+    extern __shared__ __align__(16) uint8_t smem[];
+    const int lane = threadIdx.x & 31;
+    const int warp = threadIdx.x >> 5;
+    Geo g;
+    if (!parse_header(a, g)) return;
     const DecSlot S = dec_slot(g.cs, g.E);
     const int slots = (int)(kDecSmem / S.total) < kDecWarps ? (int)(kDecSmem / S.total) : kDecWarps;
     if (warp >= slots) return;
@@ -368,6 +351,7 @@ __global__ void __launch_bounds__(kDecWarps * 32) decode_kernel(DecodeArgs a) {
 cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t stream) {
     static int configured_dev = -1;
     static int grid_cache = 0;
+    static int sms_cache = 0;
     int dev = 0;
     cudaError_t err = cudaGetDevice(&dev);
     if (err != cudaSuccess) return err;
@@ -384,11 +368,17 @@ cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t stream) {
             cudaSuccess)
             return err;
         grid_cache = sms * (per_sm < 1 ? 1 : per_sm);
+        sms_cache = sms;
         configured_dev = dev;
     }
     // Chunks per stream are bounded by n_bytes / 1024 (the smallest chunk).
-    uint64_t max_chunks = (a.n_bytes + 1023u) / 1024u;
-    uint64_t max_ctas = (max_chunks + kDecWarps - 1) / kDecWarps;
+    const uint64_t max_chunks = (a.n_bytes + 1023u) / 1024u;
+    uint64_t tgrid = (max_chunks + kTile - 1) / kTile;
+    if (tgrid > (uint64_t)sms_cache * 4u) tgrid = (uint64_t)sms_cache * 4u;
+    if (tgrid < 1) tgrid = 1;
+    offsets_kernel<<<(unsigned)tgrid, kScanThreads, 0, stream>>>(a);
+    if ((err = cudaGetLastError()) != cudaSuccess) return err;
+    const uint64_t max_ctas = (max_chunks + kDecWarps - 1) / kDecWarps;
     uint64_t grid = (uint64_t)grid_cache;
     if (grid > max_ctas) grid = max_ctas;
     if (grid < 1) grid = 1;

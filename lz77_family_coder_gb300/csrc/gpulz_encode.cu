@@ -33,7 +33,7 @@ namespace {
 constexpr uint32_t FULL = 0xFFFFFFFFu;
 
 struct EncLayout {
-    uint32_t el, om, lo, tab, fl, path, data, misc, total;
+    uint32_t el, om, lo, tab, fl, data, misc, total;
 };
 
 __host__ __device__ inline uint32_t align16(uint32_t v) { return (v + 15u) & ~15u; }
@@ -46,8 +46,7 @@ __host__ __device__ inline EncLayout enc_layout(uint32_t cs, uint32_t E, int lev
     L.lo = o;   o = align16(o + 2u * E);                 // (len | off << 8) per position
     L.tab = o;  o = align16(o + (level ? 8u * E : 0u));  // level-1 table, 2E buckets of u32
     L.fl = o;   o = align16(o + E / 8u);                 // flag staging
-    L.path = o; o = align16(o + E / 8u);                 // on-path bitmask
-    L.data = o; o = align16(o + cs + 256u);              // item staging
+    L.data = o; o = align16(o + cs + 16u);               // block staging
     L.misc = o; o = align16(o + 256u);
     L.total = o;
     return L;
@@ -77,181 +76,30 @@ __device__ __forceinline__ uint32_t chunk_byte_addr(uint32_t b) {
 }
 
 // ---------------------------------------------------------------------------
-// Parse helpers (one warp).
+// Parse helpers.
 // ---------------------------------------------------------------------------
-// On-path lanes of a 32-position window whose first position is on the path.
-// nxt = lane + step(lane) (relative; > lane). Pointer doubling: after round r
-// the set holds the first 2^(r+1) path positions; 5 rounds cover a window.
-__device__ __forceinline__ uint32_t window_path(uint32_t nxt, int lane) {
-    uint32_t S = 1u;
-    uint32_t J = nxt;
-#pragma unroll
-    for (int r = 0; r < 5; ++r) {
-        uint32_t mine = (((S >> lane) & 1u) && J < 32u) ? (1u << J) : 0u;
-        S |= __reduce_or_sync(FULL, mine);
-        uint32_t Jn = __shfl_sync(FULL, J, J & 31u);
-        J = (J < 32u) ? Jn : J;
-    }
-    return S;
+// Step byte of relative position p (< 16) from four packed words.
+__device__ __forceinline__ uint32_t seg_step(const uint32_t (&T)[4], uint32_t p) {
+    const uint32_t lo = (p & 8u) ? T[2] : T[0];
+    const uint32_t hi = (p & 8u) ? T[3] : T[1];
+    return __byte_perm(lo, hi, p & 7u) & 0xFFu;
 }
 
-template <int WS>
-__device__ __forceinline__ uint32_t step_at(const uint16_t* s_lo, uint32_t pos, uint32_t E) {
-    if (pos >= E) return 1u;
-    uint32_t len = s_lo[pos] & 0xFFu;
-    return len >= (uint32_t)min_match_len(WS) ? len : 1u;
-}
-
-// OR `bits` (relative to position `start`) into the bitmask.
-__device__ __forceinline__ void or_bits(uint32_t* s_path, uint32_t start, uint32_t bits) {
+// OR `bits` (relative to bit position `start`) into a bitmask in shared memory.
+__device__ __forceinline__ void or_bits(uint32_t* words, uint32_t start, uint32_t bits) {
     if (!bits) return;
-    uint32_t w = start >> 5, sh = start & 31u;
-    atomicOr(&s_path[w], bits << sh);
-    if (sh && (bits >> (32u - sh))) atomicOr(&s_path[w + 1], bits >> (32u - sh));
-}
-
-// Clear bits [start, start + len) of the bitmask (warp-cooperative).
-__device__ __forceinline__ void clear_bits(uint32_t* s_path, uint32_t start, uint32_t len,
-                                           int lane) {
-    if (!len) return;
-    uint32_t end = start + len;
-    uint32_t w0 = start >> 5, w1 = (end - 1) >> 5;
-    for (uint32_t w = w0 + lane; w <= w1; w += 32) {
-        uint32_t lo = (w == w0) ? (start & 31u) : 0u;
-        uint32_t hi = (w == w1) ? ((end - 1) & 31u) : 31u;
-        uint32_t m = (hi == 31u ? FULL : ((1u << (hi + 1)) - 1u)) & ~((1u << lo) - 1u);
-        atomicAnd(&s_path[w], ~m);
-    }
-}
-
-// Walk [cur, b) from `cur` (assumed on the path), recording path bits below b.
-// Returns the first path position >= b.
-template <int WS>
-__device__ uint32_t walk_segment(uint32_t cur, uint32_t b, uint32_t E, const uint16_t* s_lo,
-                                 uint32_t* s_path, int lane) {
-    while (cur < b) {
-        uint32_t nxt = (uint32_t)lane + step_at<WS>(s_lo, cur + lane, E);
-        uint32_t S = window_path(nxt, lane);
-        uint32_t lim = b - cur;
-        uint32_t valid = lim >= 32u ? FULL : ((1u << lim) - 1u);
-        uint32_t Sin = S & valid;
-        if (lane == 0) or_bits(s_path, cur, Sin);
-        int hi = 31 - __clz(Sin);
-        cur += __shfl_sync(FULL, nxt, hi);
-        __syncwarp();
-    }
-    return cur;
-}
-
-// Repair segment [a, b) whose speculative path started at a, given the true
-// entry e >= a. Returns the true exit.
-template <int WS>
-__device__ uint32_t repair_segment(uint32_t e, uint32_t a, uint32_t b, uint32_t spec_exit,
-                                   uint32_t E, const uint16_t* s_lo, uint32_t* s_path, int lane) {
-    if (e == a) return spec_exit;
-    clear_bits(s_path, a, e - a, lane);
-    __syncwarp();
-    uint32_t cur = e;
-    while (cur < b) {
-        uint32_t nxt = (uint32_t)lane + step_at<WS>(s_lo, cur + lane, E);
-        uint32_t S = window_path(nxt, lane);
-        uint32_t lim = b - cur;
-        uint32_t valid = lim >= 32u ? FULL : ((1u << lim) - 1u);
-        uint32_t Sin = S & valid;
-        // speculative bits of [cur, cur + 32)
-        uint32_t w = cur >> 5, sh = cur & 31u;
-        uint32_t spec = s_path[w] >> sh;
-        if (sh && w + 1 < (E >> 5)) spec |= s_path[w + 1] << (32u - sh);
-        spec &= valid;
-        uint32_t I = Sin & spec;
-        __syncwarp();
-        if (I) {
-            uint32_t m = (uint32_t)__ffs(I) - 1u;  // first common position (relative)
-            clear_bits(s_path, cur, m, lane);
-            __syncwarp();
-            if (lane == 0) or_bits(s_path, cur, Sin & ((1u << m) - 1u));
-            __syncwarp();
-            return spec_exit;
-        }
-        int hi = 31 - __clz(Sin);
-        uint32_t nx = cur + __shfl_sync(FULL, nxt, hi);
-        uint32_t upto = nx < b ? nx : b;
-        clear_bits(s_path, cur, upto - cur, lane);
-        __syncwarp();
-        if (lane == 0) or_bits(s_path, cur, Sin);
-        __syncwarp();
-        cur = nx;
-    }
-    return cur;
+    const uint32_t w = start >> 5, sh = start & 31u;
+    atomicOr(&words[w], bits << sh);
+    if (sh && (bits >> (32u - sh))) atomicOr(&words[w + 1], bits >> (32u - sh));
 }
 
 // ---------------------------------------------------------------------------
-// Look-back (warp 0): exclusive prefix of block bytes over earlier chunks.
+// Single-pass placement (used by the allocation-free entry point): chunk c
+// publishes its block size, and its offset is the exclusive prefix over the
+// chunk descriptors by decoupled look-back (lookback() in gpulz_internal.cuh).
 // ---------------------------------------------------------------------------
-__device__ __forceinline__ void publish_aggregate(const EncodeArgs& a, uint32_t c,
-                                                  uint64_t aggregate) {
-    st_relaxed_u64(&a.desc[c],
-                   make_desc(a.epoch, c == 0 ? kDescInclusive : kDescAggregate, aggregate));
-}
-
-// Exclusive prefix of block bytes over chunks [0, c) by decoupled look-back.
-// The warp inspects kLookBackWidth predecessors per step (each lane loads
-// kLookBackPerLane descriptors, so the loads overlap): it sums aggregates back
-// to the nearest inclusive prefix. The aggregate of chunk c must already be
-// published. Waits are bounded by kWaitLimitNs of device time.
-constexpr int kLookBackPerLane = 8;
-constexpr int kLookBackWidth = 32 * kLookBackPerLane;
-
-__device__ uint64_t lookback_encode(const EncodeArgs& a, uint32_t c, uint64_t aggregate, int lane,
-                                    bool* timed_out) {
-    *timed_out = false;
-    if (c == 0) return 0;
-    const uint64_t* desc = a.desc;
-    uint64_t prefix = 0;
-    int64_t base = (int64_t)c - 1;
-    uint64_t t0 = 0;
-    for (;;) {
-        uint64_t d[kLookBackPerLane];
-#pragma unroll
-        for (int k = 0; k < kLookBackPerLane; ++k) {
-            int64_t idx = base - (k * 32 + lane);
-            d[k] = idx >= 0 ? ld_relaxed_u64(&desc[idx]) : make_desc(a.epoch, kDescInclusive, 0);
-        }
-        uint32_t my_min = 0xFFFFFFFFu;
-#pragma unroll
-        for (int k = kLookBackPerLane - 1; k >= 0; --k) {
-            bool incl = desc_epoch(d[k]) == a.epoch && desc_kind(d[k]) == kDescInclusive;
-            if (incl) my_min = (uint32_t)(k * 32 + lane);
-        }
-        const uint32_t dmin = __reduce_min_sync(FULL, my_min);
-        const uint32_t lim = dmin == 0xFFFFFFFFu ? (uint32_t)kLookBackWidth : dmin + 1u;
-        bool bad = false;
-        uint64_t v = 0;
-#pragma unroll
-        for (int k = 0; k < kLookBackPerLane; ++k) {
-            if ((uint32_t)(k * 32 + lane) < lim) {
-                bool valid = desc_epoch(d[k]) == a.epoch && desc_kind(d[k]) != 0;
-                bad |= !valid;
-                v += desc_value(d[k]);
-            }
-        }
-        if (__any_sync(FULL, bad)) {
-            uint64_t now = globaltimer_ns();
-            if (t0 == 0) t0 = now;
-            if (now - t0 > kWaitLimitNs) {
-                *timed_out = true;
-                break;
-            }
-            __nanosleep(32);
-            continue;
-        }
-        prefix += warp_sum_u64(v);
-        if (dmin != 0xFFFFFFFFu) break;
-        base -= kLookBackWidth;
-    }
-    if (lane == 0)
-        st_relaxed_u64(&a.desc[c], make_desc(a.epoch, kDescInclusive, prefix + aggregate));
-    return prefix;
+__device__ __forceinline__ void publish_size(const EncodeArgs& a, uint32_t c, uint32_t blk) {
+    st_relaxed_u64(&a.desc[c], make_desc(a.epoch, c == 0 ? kDescInclusive : kDescAggregate, blk));
 }
 
 __device__ void store_u32_capped(uint8_t* out, uint64_t off, uint32_t v, uint64_t cap) {
@@ -274,10 +122,58 @@ __device__ void write_header(const EncodeArgs& a, uint32_t ws, uint64_t total) {
 }
 
 // ---------------------------------------------------------------------------
+// Per-segment near masks (E3): m[p] bit o-1 set iff element (base+p) equals
+// element (base+p-o), 1 <= o <= 32, base+p-o >= 0.
+// ---------------------------------------------------------------------------
+template <int WS, int SEGP>
+__device__ __forceinline__ void near_masks(const uint8_t* s_el, uint32_t base, uint32_t (&m)[SEGP]) {
+    // Eight positions at a time: their 32-element window and themselves are
+    // 40 elements, loaded as ten aligned 4-element vectors.
+#pragma unroll
+    for (int h = 0; h < SEGP / 8; ++h) {
+        const int first = (int)base + 8 * h - 32;  // a multiple of 4
+        uint32_t v[40];
+#pragma unroll
+        for (int q = 0; q < 10; ++q) {
+            const int i0 = first + 4 * q;
+            uint32_t w[4] = {0u, 0u, 0u, 0u};
+            if (i0 >= 0) {
+                const uint8_t* p = s_el + el_addr<WS>((uint32_t)i0);
+                if (WS == 4) {
+                    const uint4 t = *reinterpret_cast<const uint4*>(p);
+                    w[0] = t.x; w[1] = t.y; w[2] = t.z; w[3] = t.w;
+                } else if (WS == 2) {
+                    const uint2 t = *reinterpret_cast<const uint2*>(p);
+                    w[0] = t.x & 0xFFFFu; w[1] = t.x >> 16; w[2] = t.y & 0xFFFFu; w[3] = t.y >> 16;
+                } else {
+                    const uint32_t t = *reinterpret_cast<const uint32_t*>(p);
+                    w[0] = t & 0xFFu; w[1] = (t >> 8) & 0xFFu; w[2] = (t >> 16) & 0xFFu; w[3] = t >> 24;
+                }
+            }
+#pragma unroll
+            for (int r = 0; r < 4; ++r) v[4 * q + r] = w[r];
+        }
+#pragma unroll
+        for (int p = 0; p < 8; ++p) {
+            const uint32_t x = v[32 + p];
+            uint32_t mm = 0;
+#pragma unroll
+            for (int o = 1; o <= 32; ++o) mm |= (v[32 + p - o] == x) ? (1u << (o - 1)) : 0u;
+            const uint32_t i = base + (uint32_t)(8 * h + p);
+            if (i < 32u) mm &= (1u << i) - 1u;
+            m[8 * h + p] = mm;
+        }
+    }
+}
+
+// 4 bits -> 4 bytes of 0/1.
+__device__ __forceinline__ uint32_t expand4(uint32_t bits) { return (bits * 0x00204081u) & 0x01010101u; }
+
+// ---------------------------------------------------------------------------
 // The kernel.
 // ---------------------------------------------------------------------------
-template <int WS, int LEVEL>
-__global__ void __launch_bounds__(256) encode_kernel(EncodeArgs a) {
+template <int WS, int LEVEL, int SEGP, bool SINGLE>
+__global__ void __launch_bounds__(256, 4) encode_kernel(EncodeArgs a) {
     extern __shared__ __align__(16) uint8_t smem[];
     const int tid = threadIdx.x;
     const int lane = tid & 31;
@@ -292,10 +188,10 @@ __global__ void __launch_bounds__(256) encode_kernel(EncodeArgs a) {
     uint16_t* s_lo = reinterpret_cast<uint16_t*>(smem + L.lo);
     uint32_t* s_tab = reinterpret_cast<uint32_t*>(smem + L.tab);
     uint32_t* s_fl = reinterpret_cast<uint32_t*>(smem + L.fl);
-    uint32_t* s_path = reinterpret_cast<uint32_t*>(smem + L.path);
     uint8_t* s_data = smem + L.data;
     uint32_t* s_misc = reinterpret_cast<uint32_t*>(smem + L.misc);
     constexpr uint32_t LMIN = (uint32_t)min_match_len(WS);
+    constexpr uint32_t NONE = 0xFFFFFFFFu;
 
     if (a.n_chunks == 0) {
         if (blockIdx.x == 0 && tid == 0) write_header(a, WS, kHeaderBytes);
@@ -303,325 +199,517 @@ __global__ void __launch_bounds__(256) encode_kernel(EncodeArgs a) {
     }
     const uint64_t body0 = (uint64_t)kHeaderBytes + (uint64_t)kEntryBytes * a.n_chunks;
     const bool in_aligned = (reinterpret_cast<uintptr_t>(a.in) & 15u) == 0;
+    const uint32_t seg_a = (uint32_t)tid * SEGP;  // this thread's positions [seg_a, seg_a + SEGP)
+
+    // The chunk staged in s_fl/s_data whose offset is not known yet. Its
+    // look-back runs after the next chunk's match search, by which time its
+    // predecessors have published their sizes, so the wait is normally empty.
+    uint32_t p_c = NONE, p_blk = 0, p_entry = 0, p_dbytes = 0, p_fw = 0, p_dw = 0;
 
     for (;;) {
         if (tid == 0) s_misc[0] = atomicAdd(a.ticket, 1u);
         __syncthreads();
-        const uint32_t c = s_misc[0];
-        if (c >= a.n_chunks) break;
+        const uint32_t t = s_misc[0];
+        const bool have = t < a.n_chunks;
+        // Single pass: chunks in ticket order (the look-back needs it). Two
+        // pass: the zero-padded tail chunk first, as it is often the slowest.
+        const uint32_t c = (SINGLE || !have) ? t : (t == 0 ? a.n_chunks - 1u : t - 1u);
 
-        // ---- E1: load the chunk (zero padded) ----
-        const uint64_t begin = (uint64_t)c * CS;
-        const uint64_t avail = a.n_bytes - begin;
-        const uint32_t take = avail < CS ? (uint32_t)avail : CS;
-        uint32_t nz = 0;
-        if (in_aligned && take == CS) {
-            const uint4* src = reinterpret_cast<const uint4*>(a.in + begin);
-            for (uint32_t g = tid; g < CS / 16u; g += nthreads) {
-                uint4 v = __ldg(src + g);
-                uint32_t* dst = reinterpret_cast<uint32_t*>(s_el + chunk_byte_addr<WS>(16u * g));
-                dst[0] = v.x; dst[1] = v.y; dst[2] = v.z; dst[3] = v.w;
-                nz |= v.x | v.y | v.z | v.w;
-            }
-        } else {
-            for (uint32_t b4 = tid; b4 < CS / 4u; b4 += nthreads) {
-                uint32_t v = 0;
-                for (uint32_t k = 0; k < 4u; ++k) {
-                    uint32_t b = 4u * b4 + k;
-                    if (b < take) v |= (uint32_t)a.in[begin + b] << (8u * k);
-                }
-                *reinterpret_cast<uint32_t*>(s_el + chunk_byte_addr<WS>(4u * b4)) = v;
-                nz |= v;
-            }
-        }
-        // clear per-chunk state
-        for (uint32_t k = tid; k < E / 32u; k += nthreads) {
-            s_fl[k] = 0;
-            s_path[k] = 0;
-        }
-        if (LEVEL) {
-            for (uint32_t k = tid; k < 2u * E; k += nthreads) s_tab[k] = 0;
-        }
-        // ---- E2: zero test ----
-        const bool nonzero = __syncthreads_or(nz != 0) != 0;
-
+        bool nonzero = false;
         uint32_t items = 0, dbytes = 0, blk = 0, entry_items = 0;
-        if (nonzero) {
-            // ---- E3: near equality masks, 16 positions per thread step ----
-            for (uint32_t g = tid; g < E / 16u; g += nthreads) {
-                uint32_t v[48];
-#pragma unroll
-                for (int h = 0; h < 3; ++h) {
-                    int grp = (int)g - 2 + h;
-                    if (grp < 0) {
-#pragma unroll
-                        for (int k = 0; k < 16; ++k) v[16 * h + k] = 0;
-                        continue;
-                    }
-                    const uint4* p = reinterpret_cast<const uint4*>(s_el + el_addr<WS>(16u * grp));
-#pragma unroll
-                    for (int q = 0; q < WS; ++q) {
-                        uint4 t = p[q];
-                        uint32_t wd[4] = {t.x, t.y, t.z, t.w};
-#pragma unroll
-                        for (int r = 0; r < 4; ++r) {
-                            if (WS == 4) {
-                                v[16 * h + 4 * q + r] = wd[r];
-                            } else if (WS == 2) {
-                                v[16 * h + 8 * q + 2 * r] = wd[r] & 0xFFFFu;
-                                v[16 * h + 8 * q + 2 * r + 1] = wd[r] >> 16;
-                            } else {
-#pragma unroll
-                                for (int s = 0; s < 4; ++s)
-                                    v[16 * h + 16 * q + 4 * r + s] = (wd[r] >> (8 * s)) & 0xFFu;
-                            }
-                        }
-                    }
-                }
-                uint32_t m[16];
-#pragma unroll
-                for (int p = 0; p < 16; ++p) {
-                    uint32_t x = v[32 + p];
-                    uint32_t mm = 0;
-#pragma unroll
-                    for (int o = 1; o <= 32; ++o) mm |= (v[32 + p - o] == x) ? (1u << (o - 1)) : 0u;
-                    uint32_t i = 16u * g + (uint32_t)p;
-                    if (i < 32u) mm &= (1u << i) - 1u;
-                    m[p] = mm;
-                }
-                uint4* dst = reinterpret_cast<uint4*>(s_om + om_idx(16u * g));
-#pragma unroll
-                for (int q = 0; q < 4; ++q)
-                    dst[q] = make_uint4(m[4 * q], m[4 * q + 1], m[4 * q + 2], m[4 * q + 3]);
-            }
-            __syncthreads();
-
-            // ---- E4: AND-chain longest match, nearest offset ----
-            for (uint32_t i = tid; i < E; i += nthreads) {
-                uint32_t mm = s_om[om_idx(i)];
-                uint32_t lo = 0;
-                if (mm) {
-                    uint32_t cap = E - i < (uint32_t)kMaxLen ? E - i : (uint32_t)kMaxLen;
-                    uint32_t len = 1;
-                    while (len < cap) {
-                        uint32_t nm = mm & s_om[om_idx(i + len)];
-                        if (!nm) break;
-                        mm = nm;
-                        ++len;
-                    }
-                    lo = len | ((uint32_t)__ffs(mm) << 8);
-                }
-                s_lo[i] = (uint16_t)lo;
-            }
-            __syncthreads();
-
-            // ---- E5: level-1 hashed candidates over 8 sub-blocks ----
-            if (LEVEL) {
-                const uint32_t SB = E / kSubBlocks;
-                for (int s = 0; s < kSubBlocks; ++s) {
-                    const uint32_t lo_i = (uint32_t)s * SB;
-                    for (uint32_t i = lo_i + tid; i < lo_i + SB; i += nthreads) {
-                        if (i + 1u >= E) continue;
-                        uint32_t slot = s_tab[key_hash(el_get<WS>(s_el, i), el_get<WS>(s_el, i + 1u),
-                                                       a.hash_bits)];
-                        if (!slot) continue;
-                        uint32_t p = slot - 1u;
-                        uint32_t d = i - p;
-                        if (d > (uint32_t)kMaxOff) continue;
-                        uint32_t cap = E - i < (uint32_t)kMaxLen ? E - i : (uint32_t)kMaxLen;
-                        uint32_t k = 0;
-                        while (k < cap && el_get<WS>(s_el, i + k) == el_get<WS>(s_el, p + k)) ++k;
-                        if (!k) continue;
-                        uint32_t cur = s_lo[i];
-                        uint32_t l0 = cur & 0xFFu, o0 = cur >> 8;
-                        if (k > l0 || (k == l0 && d < o0)) s_lo[i] = (uint16_t)(k | (d << 8));
-                    }
-                    __syncthreads();
-                    for (uint32_t p = lo_i + tid; p < lo_i + SB; p += nthreads) {
-                        if (p + 1u >= E) continue;
-                        atomicMax(&s_tab[key_hash(el_get<WS>(s_el, p), el_get<WS>(s_el, p + 1u),
-                                                  a.hash_bits)],
-                                  p + 1u);
-                    }
-                    __syncthreads();
-                }
-            }
-
-            // ---- E6: greedy parse -> on-path bitmask ----
-            const uint32_t SEG = E / (uint32_t)nwarps;
-            {
-                uint32_t sa = (uint32_t)warp * SEG;
-                uint32_t ex = walk_segment<WS>(sa, sa + SEG, E, s_lo, s_path, lane);
-                if (lane == 0) s_misc[8 + warp] = ex;
-            }
-            __syncthreads();
-            if (nwarps > 1 && warp == 0) {
-                uint32_t e = s_misc[8];
-                for (int w = 1; w < nwarps; ++w) {
-                    uint32_t sa = (uint32_t)w * SEG;
-                    e = repair_segment<WS>(e, sa, sa + SEG, s_misc[8 + w], E, s_lo, s_path, lane);
-                }
-            }
-            __syncthreads();
-
-            // ---- count items and match tokens per segment ----
-            {
-                uint32_t sa = (uint32_t)warp * SEG;
-                uint32_t n_it = 0, n_m = 0;
-                for (uint32_t bp = sa; bp < sa + SEG; bp += 32u) {
-                    uint32_t S = s_path[bp >> 5];
-                    uint32_t len = s_lo[bp + lane] & 0xFFu;
-                    bool ism = ((S >> lane) & 1u) && len >= LMIN;
-                    uint32_t M = __ballot_sync(FULL, ism);
-                    n_it += __popc(S);
-                    n_m += __popc(M);
-                }
-                if (lane == 0) {
-                    s_misc[16 + warp] = n_it;
-                    s_misc[24 + warp] = n_m;
-                }
-            }
-            __syncthreads();
-            uint32_t item_base = 0, match_base = 0;
-            for (int w = 0; w < nwarps; ++w) {
-                uint32_t ni = s_misc[16 + w], nm = s_misc[24 + w];
-                if (w < warp) {
-                    item_base += ni;
-                    match_base += nm;
-                }
-                items += ni;
-                dbytes += WS * (ni - nm) + 2u * nm;
-            }
-            blk = 4u * ((items + 31u) / 32u) + ((dbytes + 3u) & ~3u);
-            if (blk >= CS) {
-                blk = CS;
-                entry_items = kRawBit;
-                dbytes = CS;
-            }
-            // publish this chunk's size before packing, so successors' look-backs resolve early
-            if (tid == 0) publish_aggregate(a, c, blk);
-            if (entry_items != kRawBit) {
-                entry_items = items;
-                // ---- E7: emit flags + items into staging ----
-                uint32_t sa = (uint32_t)warp * SEG;
-                uint32_t ib = item_base;
-                uint32_t bb = WS * (item_base - match_base) + 2u * match_base;
-                const uint32_t lt = lanemask_lt();
-                for (uint32_t bp = sa; bp < sa + SEG; bp += 32u) {
-                    uint32_t S = s_path[bp >> 5];
-                    uint32_t pos = bp + lane;
-                    uint32_t lo = s_lo[pos];
-                    uint32_t len = lo & 0xFFu;
-                    bool onp = (S >> lane) & 1u;
-                    bool ism = onp && len >= LMIN;
-                    uint32_t M = __ballot_sync(FULL, ism);
-                    uint32_t rank = __popc(S & lt);
-                    uint32_t mb = __popc(M & lt);
-                    uint32_t boff = bb + WS * (rank - mb) + 2u * mb;
-                    if (onp) {
-                        if (ism) {
-                            if (WS == 1) {
-                                s_data[boff] = (uint8_t)len;
-                                s_data[boff + 1] = (uint8_t)(lo >> 8);
-                            } else {
-                                *reinterpret_cast<uint16_t*>(s_data + boff) = (uint16_t)lo;
-                            }
-                        } else {
-                            uint32_t v = el_get<WS>(s_el, pos);
-                            if (WS == 1) {
-                                s_data[boff] = (uint8_t)v;
-                            } else if (WS == 2) {
-                                *reinterpret_cast<uint16_t*>(s_data + boff) = (uint16_t)v;
-                            } else {
-                                *reinterpret_cast<uint16_t*>(s_data + boff) = (uint16_t)v;
-                                *reinterpret_cast<uint16_t*>(s_data + boff + 2) = (uint16_t)(v >> 16);
-                            }
-                        }
-                    }
-                    uint32_t fb = __reduce_or_sync(FULL, ism ? (1u << rank) : 0u);
-                    if (lane == 0 && fb) or_bits(s_fl, ib, fb);
-                    uint32_t n = __popc(S), nm = __popc(M);
-                    ib += n;
-                    bb += WS * (n - nm) + 2u * nm;
-                }
-            }
-        }
-        if (!nonzero && tid == 0) publish_aggregate(a, c, 0);
-        // ---- E9: look-back for this chunk's byte offset ----
-        if (warp == 0) {
-            bool to = false;
-            uint64_t prefix = lookback_encode(a, c, blk, lane, &to);
-            if (lane == 0) {
-                if (to) atomicOr(a.status, kStatTimeout);
-                s_misc[40] = (uint32_t)prefix;
-                s_misc[41] = (uint32_t)(prefix >> 32);
-            }
-        }
-        if (tid == 0 && entry_items != kRawBit && nonzero) {
-            // zero the padding bytes after the last item
-            for (uint32_t k = dbytes; k < ((dbytes + 3u) & ~3u); ++k) s_data[k] = 0;
-        }
-        __syncthreads();
-        const uint64_t prefix = (uint64_t)s_misc[40] | ((uint64_t)s_misc[41] << 32);
-
-        // ---- E10: store-out (32-bit coalesced), size-table entry, header ----
-        const uint64_t dst = body0 + prefix;
-        if (nonzero) {
-            if (entry_items == kRawBit) {
-                for (uint32_t j = tid; j < CS / 4u; j += nthreads) {
-                    uint32_t v = *reinterpret_cast<const uint32_t*>(s_el + chunk_byte_addr<WS>(4u * j));
-                    store_u32_capped(a.out, dst + 4ull * j, v, a.capacity);
+        uint32_t path = 0, mmask = 0, item_base = 0, match_base = 0;
+        if (have) {
+            // ---- E1: load the chunk (zero padded) ----
+            const uint64_t begin = (uint64_t)c * CS;
+            const uint64_t avail = a.n_bytes - begin;
+            const uint32_t take = avail < CS ? (uint32_t)avail : CS;
+            uint32_t nz = 0;
+            if (in_aligned && take == CS) {
+                const uint4* src = reinterpret_cast<const uint4*>(a.in + begin);
+                for (uint32_t g = tid; g < CS / 16u; g += nthreads) {
+                    const uint4 v = __ldg(src + g);
+                    uint32_t* dst = reinterpret_cast<uint32_t*>(s_el + chunk_byte_addr<WS>(16u * g));
+                    dst[0] = v.x; dst[1] = v.y; dst[2] = v.z; dst[3] = v.w;
+                    nz |= v.x | v.y | v.z | v.w;
                 }
             } else {
-                const uint32_t fw = (items + 31u) / 32u;
-                const uint32_t dw = (dbytes + 3u) / 4u;
-                for (uint32_t j = tid; j < fw + dw; j += nthreads) {
-                    uint32_t v = j < fw ? s_fl[j]
-                                        : *reinterpret_cast<const uint32_t*>(s_data + 4u * (j - fw));
-                    store_u32_capped(a.out, dst + 4ull * j, v, a.capacity);
+                for (uint32_t b4 = tid; b4 < CS / 4u; b4 += nthreads) {
+                    uint32_t v = 0;
+                    for (uint32_t k = 0; k < 4u; ++k) {
+                        const uint32_t b = 4u * b4 + k;
+                        if (b < take) v |= (uint32_t)a.in[begin + b] << (8u * k);
+                    }
+                    *reinterpret_cast<uint32_t*>(s_el + chunk_byte_addr<WS>(4u * b4)) = v;
+                    nz |= v;
                 }
             }
+            if (LEVEL) {
+                for (uint32_t k = tid; k < 2u * E; k += nthreads) s_tab[k] = 0;
+            }
+            // ---- E2: zero test ----
+            nonzero = __syncthreads_or(nz != 0) != 0;
+
+            if (nonzero) {
+                // ---- E3: near equality masks of this thread's segment ----
+                uint32_t m[SEGP];
+                near_masks<WS, SEGP>(s_el, seg_a, m);
+                {
+                    uint4* dst = reinterpret_cast<uint4*>(s_om + om_idx(seg_a));
+#pragma unroll
+                    for (int q = 0; q < SEGP / 4; ++q)
+                        dst[q] = make_uint4(m[4 * q], m[4 * q + 1], m[4 * q + 2], m[4 * q + 3]);
+                }
+                __syncthreads();
+
+                // ---- E4: AND-chain longest match, nearest offset ----
+                // The chains of the segment's positions advance together in
+                // registers; one that is still alive at the segment end is
+                // finished from the shared-memory masks.
+                {
+                    uint32_t cc[SEGP];
+                    uint32_t A = 0;
+#pragma unroll
+                    for (int p = 0; p < SEGP; ++p) {
+                        cc[p] = m[p];
+                        A |= (uint32_t)(m[p] != 0u) << p;
+                    }
+                    uint32_t lb[SEGP / 4];
+#pragma unroll
+                    for (int w = 0; w < SEGP / 4; ++w) lb[w] = expand4((A >> (4 * w)) & 15u);
+                    uint32_t P = A & (1u << (SEGP - 1));
+#pragma unroll
+                    for (int k = 1; k < SEGP; ++k) {
+                        const uint32_t act = A & ((1u << (SEGP - k)) - 1u);
+                        if (!__any_sync(FULL, act != 0u)) break;
+                        uint32_t An = 0;
+#pragma unroll
+                        for (int p = 0; p + k < SEGP; ++p) {
+                            const uint32_t x = cc[p] & m[p + k];
+                            const bool ok = ((act >> p) & 1u) && x != 0u;
+                            cc[p] = ok ? x : cc[p];
+                            An |= (uint32_t)ok << p;
+                        }
+#pragma unroll
+                        for (int w = 0; w < SEGP / 4; ++w) lb[w] += expand4((An >> (4 * w)) & 15u);
+                        P |= An & (1u << (SEGP - 1 - k));
+                        A = An;
+                    }
+                    // Chains still alive at the segment end continue over the
+                    // following positions' masks in lockstep: one shared-memory
+                    // load per step serves all of them, so a long run costs
+                    // O(run) loads rather than O(run^2).
+                    if (P) {
+                        uint32_t A2 = P;
+                        for (uint32_t st = 0; A2 != 0u; ++st) {
+                            const uint32_t q = seg_a + (uint32_t)SEGP + st;
+                            if (q >= E) break;
+                            const uint32_t om = s_om[om_idx(q)];
+                            uint32_t An = 0;
+#pragma unroll
+                            for (int p = 0; p < SEGP; ++p) {
+                                const uint32_t x = cc[p] & om;
+                                const bool ok = ((A2 >> p) & 1u) && x != 0u;
+                                cc[p] = ok ? x : cc[p];
+                                An |= (uint32_t)ok << p;
+                            }
+#pragma unroll
+                            for (int w = 0; w < SEGP / 4; ++w) lb[w] += expand4((An >> (4 * w)) & 15u);
+                            // length of chain p is now SEGP - p + st + 1: stop at the cap
+                            const int over = (int)(SEGP + st + 1u) - kMaxLen;
+                            if (over >= 0) An &= ~((2u << (over < SEGP - 1 ? over : SEGP - 1)) - 1u);
+                            A2 = An;
+                        }
+                    }
+                    uint32_t lw[SEGP / 2];
+#pragma unroll
+                    for (int p = 0; p < SEGP; p += 2) {
+                        const uint32_t l0 = (lb[p >> 2] >> (8 * (p & 3))) & 0xFFu;
+                        const uint32_t l1 = (lb[p >> 2] >> (8 * ((p + 1) & 3))) & 0xFFu;
+                        const uint32_t lo0 = l0 ? (l0 | ((uint32_t)__ffs(cc[p]) << 8)) : 0u;
+                        const uint32_t lo1 = l1 ? (l1 | ((uint32_t)__ffs(cc[p + 1]) << 8)) : 0u;
+                        lw[p >> 1] = lo0 | (lo1 << 16);
+                    }
+                    uint4* dlo = reinterpret_cast<uint4*>(s_lo + seg_a);
+#pragma unroll
+                    for (int q = 0; q < SEGP / 8; ++q)
+                        dlo[q] = make_uint4(lw[4 * q], lw[4 * q + 1], lw[4 * q + 2], lw[4 * q + 3]);
+                }
+                __syncthreads();
+
+                // ---- E5: level-1 hashed candidates over 8 sub-blocks ----
+                if (LEVEL) {
+                    const uint32_t SB = E / kSubBlocks;
+                    for (int s = 0; s < kSubBlocks; ++s) {
+                        const uint32_t lo_i = (uint32_t)s * SB;
+                        for (uint32_t i = lo_i + tid; i < lo_i + SB; i += nthreads) {
+                            if (i + 1u >= E) continue;
+                            const uint32_t slot = s_tab[key_hash(el_get<WS>(s_el, i),
+                                                                 el_get<WS>(s_el, i + 1u), a.hash_bits)];
+                            if (!slot) continue;
+                            const uint32_t p = slot - 1u;
+                            const uint32_t d = i - p;
+                            if (d > (uint32_t)kMaxOff) continue;
+                            const uint32_t cap = E - i < (uint32_t)kMaxLen ? E - i : (uint32_t)kMaxLen;
+                            uint32_t k = 0;
+                            while (k < cap && el_get<WS>(s_el, i + k) == el_get<WS>(s_el, p + k)) ++k;
+                            if (!k) continue;
+                            const uint32_t cur = s_lo[i];
+                            const uint32_t l0 = cur & 0xFFu, o0 = cur >> 8;
+                            if (k > l0 || (k == l0 && d < o0)) s_lo[i] = (uint16_t)(k | (d << 8));
+                        }
+                        __syncthreads();
+                        for (uint32_t p = lo_i + tid; p < lo_i + SB; p += nthreads) {
+                            if (p + 1u >= E) continue;
+                            atomicMax(&s_tab[key_hash(el_get<WS>(s_el, p), el_get<WS>(s_el, p + 1u),
+                                                      a.hash_bits)],
+                                      p + 1u);
+                        }
+                        __syncthreads();
+                    }
+                }
+
+                // ---- E6: greedy parse, one SEGP-position segment per thread ----
+                // Each thread walks its segment from the segment start using its
+                // step bytes held in registers; then every thread whose true
+                // entry (the previous segment's exit) differs from the entry its
+                // path assumed re-walks from it, keeping its old path from the
+                // first common position on. This repeats until no entry changes.
+                uint32_t T[4] = {0u, 0u, 0u, 0u};  // step of each position, one byte each
+                {
+                    uint32_t lw[8];
+                    const uint4* q = reinterpret_cast<const uint4*>(s_lo + seg_a);
+                    const uint4 v0 = q[0];
+                    lw[0] = v0.x; lw[1] = v0.y; lw[2] = v0.z; lw[3] = v0.w;
+                    if (SEGP == 16) {
+                        const uint4 v1 = q[1];
+                        lw[4] = v1.x; lw[5] = v1.y; lw[6] = v1.z; lw[7] = v1.w;
+                    } else {
+                        lw[4] = lw[5] = lw[6] = lw[7] = 0u;
+                    }
+#pragma unroll
+                    for (int k = 0; k < SEGP; ++k) {
+                        const uint32_t len = (lw[k >> 1] >> (16 * (k & 1))) & 0xFFu;
+                        const bool mt = len >= LMIN;
+                        T[k >> 2] |= (mt ? len : 1u) << (8 * (k & 3));
+                        mmask |= (uint32_t)mt << k;
+                    }
+                }
+                uint32_t cur_e = 0, exit_abs;
+                {
+                    uint32_t p = 0;
+                    while (p < (uint32_t)SEGP) {
+                        path |= 1u << p;
+                        p += seg_step(T, p);
+                    }
+                    exit_abs = seg_a + p;
+                }
+                for (;;) {
+                    uint32_t prev = __shfl_up_sync(FULL, exit_abs, 1);
+                    if (lane == 31) s_misc[8 + warp] = exit_abs;
+                    __syncthreads();
+                    if (lane == 0) prev = warp == 0 ? 0u : s_misc[8 + warp - 1];
+                    const uint32_t te = prev - seg_a;  // true entry, relative
+                    const bool changed = te != cur_e;
+                    if (changed) {
+                        if (te >= (uint32_t)SEGP) {
+                            path = 0;
+                            exit_abs = prev;
+                        } else {
+                            const uint32_t old = path & ~((1u << te) - 1u);
+                            uint32_t np = 0, p = te;
+                            bool merged = false;
+                            while (p < (uint32_t)SEGP) {
+                                if ((old >> p) & 1u) {
+                                    merged = true;
+                                    break;
+                                }
+                                np |= 1u << p;
+                                p += seg_step(T, p);
+                            }
+                            if (merged) {
+                                path = np | (old & ~((1u << p) - 1u));
+                            } else {
+                                path = np;
+                                exit_abs = seg_a + p;
+                            }
+                        }
+                        cur_e = te;
+                    }
+                    if (!__syncthreads_or(changed)) break;
+                }
+
+                // ---- E7 (sizes): team scan of item and match counts ----
+                {
+                    const uint32_t x =
+                        (uint32_t)__popc(path) | ((uint32_t)__popc(path & mmask) << 16);
+                    uint32_t incl = x;
+#pragma unroll
+                    for (int o = 1; o < 32; o <<= 1) {
+                        const uint32_t t = __shfl_up_sync(FULL, incl, o);
+                        if (lane >= o) incl += t;
+                    }
+                    if (lane == 31) s_misc[16 + warp] = incl;
+                    __syncthreads();
+                    uint32_t wbase = 0, total = 0;
+                    for (int w = 0; w < nwarps; ++w) {
+                        const uint32_t v = s_misc[16 + w];
+                        if (w < warp) wbase += v;
+                        total += v;
+                    }
+                    const uint32_t excl = wbase + incl - x;
+                    item_base = excl & 0xFFFFu;
+                    match_base = excl >> 16;
+                    items = total & 0xFFFFu;
+                    const uint32_t matches = total >> 16;
+                    dbytes = WS * (items - matches) + 2u * matches;
+                }
+                // ---- E8: raw fallback ----
+                blk = 4u * ((items + 31u) / 32u) + ((dbytes + 3u) & ~3u);
+                if (blk >= CS) {
+                    blk = CS;
+                    entry_items = kRawBit;
+                    dbytes = CS;
+                } else {
+                    entry_items = items;
+                }
+            }
+            // publish this chunk's size now, so successors' look-backs resolve early
+            if (SINGLE && tid == 0) publish_size(a, c, blk);
         }
-        if (tid == 0) {
-            uint64_t eo = (uint64_t)kHeaderBytes + (uint64_t)kEntryBytes * c;
-            store_u32_capped(a.out, eo, nonzero ? entry_items : 0u, a.capacity);
-            store_u32_capped(a.out, eo + 4, nonzero ? dbytes : 0u, a.capacity);
-            if (c == a.n_chunks - 1u) write_header(a, WS, dst + blk);
+
+        // ---- E9 + E10 for the pending chunk: offset, store-out, table, header ----
+        if (SINGLE && p_c != NONE) {
+            if (warp == 0) {
+                bool to = false;
+                const uint64_t prefix = p_c == 0 ? 0ull : lookback(a.desc, p_c, p_blk, a.epoch, lane, &to);
+                if (lane == 0) {
+                    if (to) atomicOr(a.status, kStatTimeout);
+                    s_misc[40] = (uint32_t)prefix;
+                    s_misc[41] = (uint32_t)(prefix >> 32);
+                }
+            }
+            __syncthreads();
+            const uint64_t prefix = (uint64_t)s_misc[40] | ((uint64_t)s_misc[41] << 32);
+            const uint64_t dst = body0 + prefix;
+            for (uint32_t j = tid; j < p_fw + p_dw; j += nthreads) {
+                const uint32_t v = j < p_fw ? s_fl[j]
+                                            : *reinterpret_cast<const uint32_t*>(s_data + 4u * (j - p_fw));
+                store_u32_capped(a.out, dst + 4ull * j, v, a.capacity);
+            }
+            if (tid == 0) {
+                const uint64_t eo = (uint64_t)kHeaderBytes + (uint64_t)kEntryBytes * p_c;
+                store_u32_capped(a.out, eo, p_entry, a.capacity);
+                store_u32_capped(a.out, eo + 4, p_dbytes, a.capacity);
+                if (p_c == a.n_chunks - 1u) write_header(a, WS, dst + p_blk);
+            }
+            __syncthreads();  // staging is free again
         }
+        if (!have) break;
+
+        // ---- E7: stage this chunk's block ----
+        uint32_t fw = 0, dw = 0;
+        if (nonzero) {
+            if (entry_items == kRawBit) {
+                dw = CS / 4u;
+                for (uint32_t j = tid; j < dw; j += nthreads)
+                    *reinterpret_cast<uint32_t*>(s_data + 4u * j) =
+                        *reinterpret_cast<const uint32_t*>(s_el + chunk_byte_addr<WS>(4u * j));
+            } else {
+                fw = (items + 31u) / 32u;
+                dw = (dbytes + 3u) / 4u;
+                for (uint32_t k = tid; k < fw; k += nthreads) s_fl[k] = 0;
+                __syncthreads();
+                uint32_t bb = WS * (item_base - match_base) + 2u * match_base;
+                uint32_t fbits = 0, k = 0, rem = path;
+                while (rem) {
+                    const uint32_t p = (uint32_t)__ffs(rem) - 1u;
+                    rem &= rem - 1u;
+                    const uint32_t pos = seg_a + p;
+                    if ((mmask >> p) & 1u) {
+                        const uint32_t lo = s_lo[pos];
+                        if (WS == 1) {
+                            s_data[bb] = (uint8_t)lo;
+                            s_data[bb + 1] = (uint8_t)(lo >> 8);
+                        } else {
+                            *reinterpret_cast<uint16_t*>(s_data + bb) = (uint16_t)lo;
+                        }
+                        bb += 2u;
+                        fbits |= 1u << k;
+                    } else {
+                        const uint32_t v = el_get<WS>(s_el, pos);
+                        if (WS == 1) {
+                            s_data[bb] = (uint8_t)v;
+                        } else if (WS == 2) {
+                            *reinterpret_cast<uint16_t*>(s_data + bb) = (uint16_t)v;
+                        } else {
+                            *reinterpret_cast<uint16_t*>(s_data + bb) = (uint16_t)v;
+                            *reinterpret_cast<uint16_t*>(s_data + bb + 2) = (uint16_t)(v >> 16);
+                        }
+                        bb += WS;
+                    }
+                    ++k;
+                }
+                if (fbits) or_bits(s_fl, item_base, fbits);
+                if (tid == 0)
+                    for (uint32_t z = dbytes; z < ((dbytes + 3u) & ~3u); ++z) s_data[z] = 0;
+            }
+        }
+        p_c = c;
+        p_blk = blk;
+        p_entry = nonzero ? entry_items : 0u;
+        p_dbytes = nonzero ? dbytes : 0u;
+        p_fw = fw;
+        p_dw = dw;
+        __syncthreads();
+        if (!SINGLE) {
+            // ---- E10 (two pass): block to its slot, size and table entry ----
+            uint8_t* slot = a.slots + (uint64_t)c * CS;
+            for (uint32_t j = tid; j < fw + dw; j += nthreads) {
+                const uint32_t v = j < fw ? s_fl[j]
+                                          : *reinterpret_cast<const uint32_t*>(s_data + 4u * (j - fw));
+                *reinterpret_cast<uint32_t*>(slot + 4u * j) = v;
+            }
+            if (tid == 0) {
+                a.sizes[c] = blk;
+                const uint64_t eo = (uint64_t)kHeaderBytes + (uint64_t)kEntryBytes * c;
+                store_u32_capped(a.out, eo, p_entry, a.capacity);
+                store_u32_capped(a.out, eo + 4, p_dbytes, a.capacity);
+            }
+            __syncthreads();  // staging is free again
+        }
+    }
+}
+
+// ---------------------------------------------------------------------------
+// Pack pass (two pass). offsets_pass: a CTA per tile of kTile chunks scans
+// their sizes and finds the tile's stream offset by look-back over tile
+// descriptors; it writes every chunk's block offset, and the last tile the
+// header and the stream length. copy_pass: one warp per chunk moves the block
+// from its slot to its offset (16-byte loads, 32-bit stores, nothing at or
+// past capacity).
+// ---------------------------------------------------------------------------
+__global__ void __launch_bounds__(kScanThreads) offsets_pass(EncodeArgs a, uint32_t ws) {
+    __shared__ TileSmem sm;
+    const int tid = threadIdx.x;
+    const uint32_t n_tiles = (a.n_chunks + kTile - 1) / kTile;
+    if (a.n_chunks == 0) {
+        if (blockIdx.x == 0 && tid == 0) write_header(a, ws, kHeaderBytes);
+        return;
+    }
+    const uint64_t body0 = (uint64_t)kHeaderBytes + (uint64_t)kEntryBytes * a.n_chunks;
+    for (;;) {
+        if (tid == 0) sm.tile = atomicAdd(a.ticket2, 1u);
+        __syncthreads();
+        const uint32_t t = sm.tile;
+        if (t >= n_tiles) break;
+        const uint64_t prefix = tile_scan(sm, t, a.n_chunks, a.tdesc, a.epoch, a.status,
+                                          [&](uint32_t c) { return a.sizes[c]; });
+        const uint32_t c0 = t * kTile;
+        for (uint32_t j = (uint32_t)tid; j < kTile && c0 + j < a.n_chunks; j += kScanThreads)
+            a.offsets[c0 + j] = body0 + prefix + sm.off[j];
+        if (t == n_tiles - 1 && tid == 0) write_header(a, ws, body0 + prefix + sm.total);
         __syncthreads();
     }
 }
 
-template <int WS, int LEVEL>
-cudaError_t launch_t(const EncodeArgs& a, cudaStream_t stream) {
-    const EncLayout L = enc_layout(a.chunk_size, a.elems, LEVEL);
-    const int threads = 32 * team_warps(a.elems);
-    auto kern = encode_kernel<WS, LEVEL>;
-    cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                           (int)L.total);
+constexpr int kCopyWarps = 8;
+
+__global__ void __launch_bounds__(kCopyWarps * 32) copy_pass(EncodeArgs a) {
+    const int lane = threadIdx.x & 31;
+    const uint32_t gw = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+    const uint32_t nw = (gridDim.x * blockDim.x) >> 5;
+    for (uint32_t c = gw; c < a.n_chunks; c += nw) {
+        const uint32_t blk = a.sizes[c];
+        const uint64_t dst = a.offsets[c];
+        const uint8_t* src = a.slots + (uint64_t)c * a.chunk_size;
+        for (uint32_t i = 16u * lane; i < blk; i += 512u) {
+            const uint4 v = *reinterpret_cast<const uint4*>(src + i);
+            const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+            for (int k = 0; k < 4; ++k)
+                if (i + 4u * k < blk) store_u32_capped(a.out, dst + i + 4u * k, w[k], a.capacity);
+        }
+    }
+}
+
+struct LaunchShape {
+    int dev = -1;
+    uint32_t smem = 0;
+    int sms = 0;
+    int per_sm = 0;
+};
+
+// Occupancy-derived grid for a kernel, cached per (device, shared memory).
+template <typename K>
+cudaError_t shape_for(K kern, int threads, uint32_t smem, LaunchShape& cache) {
+    int dev = 0;
+    cudaError_t err = cudaGetDevice(&dev);
     if (err != cudaSuccess) return err;
-    int dev = 0, sms = 0, per_sm = 0;
-    if ((err = cudaGetDevice(&dev)) != cudaSuccess) return err;
-    if ((err = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess)
-        return err;
-    if ((err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, threads, L.total)) !=
+    if (cache.dev == dev && cache.smem == smem) return cudaSuccess;
+    if ((err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem)) !=
         cudaSuccess)
         return err;
-    if (per_sm < 1) per_sm = 1;
-    uint64_t grid = (uint64_t)sms * (uint64_t)per_sm;
+    int sms = 0, per_sm = 0;
+    if ((err = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess)
+        return err;
+    if ((err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, threads, smem)) !=
+        cudaSuccess)
+        return err;
+    cache.dev = dev;
+    cache.smem = smem;
+    cache.sms = sms;
+    cache.per_sm = per_sm < 1 ? 1 : per_sm;
+    return cudaSuccess;
+}
+
+template <int WS, int LEVEL, bool SINGLE>
+cudaError_t launch_t(const EncodeArgs& a, cudaStream_t stream) {
+    static thread_local LaunchShape shape16, shape8, shape_copy;
+    const EncLayout L = enc_layout(a.chunk_size, a.elems, LEVEL);
+    const int threads = 32 * team_warps(a.elems);
+    // positions per thread: 16, except 8 for 256-element chunks
+    const bool s16 = a.elems / (uint32_t)threads == 16u;
+    auto kern = s16 ? encode_kernel<WS, LEVEL, 16, SINGLE> : encode_kernel<WS, LEVEL, 8, SINGLE>;
+    LaunchShape& shape = s16 ? shape16 : shape8;
+    cudaError_t err = shape_for(kern, threads, L.total, shape);
+    if (err != cudaSuccess) return err;
+    uint64_t grid = (uint64_t)shape.sms * (uint64_t)shape.per_sm;
     if (grid > a.n_chunks) grid = a.n_chunks;
     if (grid < 1) grid = 1;
     kern<<<(unsigned)grid, threads, L.total, stream>>>(a);
-    return cudaGetLastError();
+    if ((err = cudaGetLastError()) != cudaSuccess) return err;
+    if (!SINGLE) {
+        const uint64_t tiles = (a.n_chunks + kTile - 1) / kTile;
+        uint64_t sgrid = (uint64_t)shape.sms * 4u;
+        if (sgrid > tiles) sgrid = tiles;
+        if (sgrid < 1) sgrid = 1;
+        offsets_pass<<<(unsigned)sgrid, kScanThreads, 0, stream>>>(a, (uint32_t)WS);
+        if ((err = cudaGetLastError()) != cudaSuccess) return err;
+        if (a.n_chunks > 0) {
+            if ((err = shape_for(copy_pass, kCopyWarps * 32, 0, shape_copy)) != cudaSuccess)
+                return err;
+            uint64_t cgrid = (uint64_t)shape_copy.sms * (uint64_t)shape_copy.per_sm;
+            const uint64_t need = (a.n_chunks + kCopyWarps - 1) / kCopyWarps;
+            if (cgrid > need) cgrid = need;
+            copy_pass<<<(unsigned)cgrid, kCopyWarps * 32, 0, stream>>>(a);
+            err = cudaGetLastError();
+        }
+    }
+    return err;
 }
 
 }  // namespace
 
-cudaError_t launch_encode(const EncodeArgs& a, int word_size, int match_level,
+cudaError_t launch_encode(const EncodeArgs& a, int word_size, int match_level, bool single_pass,
                           cudaStream_t stream) {
-    if (word_size == 4) return match_level ? launch_t<4, 1>(a, stream) : launch_t<4, 0>(a, stream);
-    if (word_size == 2) return match_level ? launch_t<2, 1>(a, stream) : launch_t<2, 0>(a, stream);
-    return match_level ? launch_t<1, 1>(a, stream) : launch_t<1, 0>(a, stream);
+    if (single_pass) {
+        if (word_size == 4) return match_level ? launch_t<4, 1, true>(a, stream) : launch_t<4, 0, true>(a, stream);
+        if (word_size == 2) return match_level ? launch_t<2, 1, true>(a, stream) : launch_t<2, 0, true>(a, stream);
+        return match_level ? launch_t<1, 1, true>(a, stream) : launch_t<1, 0, true>(a, stream);
+    }
+    if (word_size == 4) return match_level ? launch_t<4, 1, false>(a, stream) : launch_t<4, 0, false>(a, stream);
+    if (word_size == 2) return match_level ? launch_t<2, 1, false>(a, stream) : launch_t<2, 0, false>(a, stream);
+    return match_level ? launch_t<1, 1, false>(a, stream) : launch_t<1, 0, false>(a, stream);
 }
 
 }  // namespace gpulz

@@ -33,12 +33,34 @@ constexpr uint32_t kStatCapacity = 4u;
 constexpr uint32_t kStatSizeMismatch = 8u;
 
 // ---- per-(device, stream) scratch layout ----
-// [0, 256)                 status word (u32 at 0)
-// [256, 256 + 4*65536)     one ticket counter per epoch (epoch in [1, 65535])
-// [kDescOffset, ...)       look-back descriptors, u64 per chunk
+// [0, 256)                    status word (u32 at 0)
+// [256, 256 + 8*65536)        two ticket counters per epoch (epoch in [1, 65535])
+// [kStateOffset, ...)         scratch_regions(): tile descriptors, per-chunk words,
+//                             block slots
 constexpr uint32_t kEpochs = 65536u;
 constexpr size_t kTicketOffset = 256;
-constexpr size_t kDescOffset = kTicketOffset + sizeof(uint32_t) * kEpochs;
+constexpr size_t kStateOffset = kTicketOffset + 2 * sizeof(uint32_t) * kEpochs;
+
+// Scan tiles: one CTA of kScanThreads threads covers kTile chunks.
+constexpr int kScanThreads = 256;
+constexpr int kScanPerThread = 4;
+constexpr uint32_t kTile = kScanThreads * kScanPerThread;
+
+struct ScratchRegions {
+    size_t tdesc, offsets, sizes, slots, end;  // byte offsets from the state base
+};
+// cap_chunks: chunks the per-chunk arrays can hold; slot_bytes: bytes of block
+// slots (chunks x chunk_size for the two-pass encode, 0 otherwise).
+__host__ __device__ constexpr ScratchRegions scratch_regions(uint64_t cap_chunks,
+                                                            uint64_t slot_bytes) {
+    ScratchRegions r{};
+    r.tdesc = 0;
+    r.offsets = 8 * (cap_chunks / kTile + 2);         // u64 per chunk
+    r.sizes = r.offsets + 8 * cap_chunks;             // u32 per chunk
+    r.slots = (r.sizes + 4 * cap_chunks + 255) & ~(size_t)255;
+    r.end = r.slots + slot_bytes;
+    return r;
+}
 
 // Descriptor: [63:48] epoch, [47:46] kind, [45:0] value (bytes).
 constexpr uint64_t kDescAggregate = 1ull;
@@ -90,13 +112,191 @@ __host__ __device__ inline uint32_t log2_exact(uint32_t v) {
     return b;
 }
 
+// ---- decoupled look-back over an array of descriptors (one warp) ----
+constexpr int kLBPerLane = 8;  // 32 lanes x 8 descriptors per step
+constexpr uint32_t kLBWidth = 32u * kLBPerLane;
+
+struct LBStep {
+    uint64_t sum;
+    bool found;
+    bool wait;
+    uint32_t first_bad;  // smallest distance not yet published (when wait)
+};
+
+// One step over arr[top - dist], dist in [0, count) (count <= kLBWidth); an
+// index below 0 reads as an inclusive prefix of 0. Sums the values back to
+// (and including) the nearest inclusive prefix, or all `count` if none.
+__device__ __forceinline__ LBStep lb_step(const uint64_t* arr, int64_t top, uint32_t count,
+                                          uint32_t epoch, int lane) {
+    uint64_t d[kLBPerLane];
+#pragma unroll
+    for (int k = 0; k < kLBPerLane; ++k) {
+        const uint32_t dist = (uint32_t)(k * 32 + lane);
+        const int64_t idx = top - (int64_t)dist;
+        d[k] = dist >= count ? 0ull
+                             : (idx >= 0 ? ld_relaxed_u64(arr + idx)
+                                         : make_desc(epoch, kDescInclusive, 0));
+    }
+    uint32_t my_min = 0xFFFFFFFFu;
+#pragma unroll
+    for (int k = kLBPerLane - 1; k >= 0; --k) {
+        const uint32_t dist = (uint32_t)(k * 32 + lane);
+        if (dist < count && desc_epoch(d[k]) == epoch && desc_kind(d[k]) == kDescInclusive)
+            my_min = dist;
+    }
+    const uint32_t dmin = __reduce_min_sync(0xFFFFFFFFu, my_min);
+    const uint32_t lim = dmin == 0xFFFFFFFFu ? count : dmin + 1u;
+    uint32_t my_bad = 0xFFFFFFFFu;
+    uint64_t v = 0;
+#pragma unroll
+    for (int k = kLBPerLane - 1; k >= 0; --k) {
+        const uint32_t dist = (uint32_t)(k * 32 + lane);
+        if (dist < lim) {
+            if (!(desc_epoch(d[k]) == epoch && desc_kind(d[k]) != 0)) my_bad = dist;
+            v += desc_value(d[k]);
+        }
+    }
+    LBStep r;
+    r.first_bad = __reduce_min_sync(0xFFFFFFFFu, my_bad);
+    r.wait = r.first_bad != 0xFFFFFFFFu;
+    r.found = dmin != 0xFFFFFFFFu;
+    r.sum = warp_sum_u64(v);
+    return r;
+}
+
+// Lane 0 polls one descriptor, backing off, until it carries this call's
+// epoch. Returns false if the wait gave up after kWaitLimitNs (measured from
+// *t0, set on the first wait).
+__device__ __forceinline__ bool wait_published(const uint64_t* arr, int64_t idx, uint32_t epoch,
+                                               int lane, uint64_t* t0) {
+    bool ok = true;
+    if (lane == 0) {
+        uint32_t ns = 32;
+        for (;;) {
+            const uint64_t d = ld_relaxed_u64(arr + idx);
+            if (desc_epoch(d) == epoch && desc_kind(d) != 0) break;
+            const uint64_t now = globaltimer_ns();
+            if (*t0 == 0) *t0 = now;
+            if (now - *t0 > kWaitLimitNs) {
+                ok = false;
+                break;
+            }
+            __nanosleep(ns);
+            if (ns < 1024) ns <<= 1;
+        }
+    }
+    return __shfl_sync(0xFFFFFFFFu, ok ? 1 : 0, 0) != 0;
+}
+
+// Exclusive prefix of `value` over entries [0, idx) of arr (one warp). The
+// caller has published arr[idx] (aggregate). Publishes arr[idx]'s inclusive
+// prefix. Every wait is on entries with smaller tickets, which publish their
+// aggregates without waiting.
+__device__ __forceinline__ uint64_t lookback(uint64_t* arr, uint32_t idx, uint64_t value,
+                                             uint32_t epoch, int lane, bool* timed_out) {
+    *timed_out = false;
+    uint64_t prefix = 0;
+    int64_t top = (int64_t)idx - 1;
+    uint64_t t0 = 0;
+    while (top >= 0) {
+        const LBStep r = lb_step(arr, top, kLBWidth, epoch, lane);
+        if (r.wait) {
+            if (!wait_published(arr, top - (int64_t)r.first_bad, epoch, lane, &t0)) {
+                *timed_out = true;
+                break;
+            }
+            continue;
+        }
+        prefix += r.sum;
+        if (r.found) break;
+        top -= kLBWidth;
+    }
+    if (lane == 0) st_relaxed_u64(&arr[idx], make_desc(epoch, kDescInclusive, prefix + value));
+    return prefix;
+}
+
+// Per-tile scan used by the encode pack pass and the decode offset pass: the
+// CTA (kScanThreads threads) takes the next tile ticket, computes the
+// exclusive offsets of its chunks' sizes (s_off, relative to the tile) and
+// the tile's exclusive prefix over earlier tiles (returned), by decoupled
+// look-back over tile descriptors. size_of(c) gives chunk c's block size.
+struct TileSmem {
+    uint32_t off[kTile];
+    uint32_t size[kTile];
+    uint32_t warp_sum[kScanThreads / 32];
+    uint32_t tile;
+    uint32_t total;
+    unsigned long long prefix;
+    uint32_t flags;
+};
+
+template <typename SizeFn>
+__device__ __forceinline__ uint64_t tile_scan(TileSmem& sm, uint32_t t, uint32_t n_chunks,
+                                              uint64_t* tdesc, uint32_t epoch, uint32_t* status,
+                                              SizeFn size_of) {
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const uint32_t c0 = t * kTile;
+    uint32_t v[kScanPerThread];
+    uint32_t sum = 0;
+#pragma unroll
+    for (int k = 0; k < kScanPerThread; ++k) {
+        const uint32_t c = c0 + (uint32_t)(tid * kScanPerThread + k);
+        v[k] = c < n_chunks ? size_of(c) : 0u;
+        sum += v[k];
+    }
+    uint32_t incl = sum;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const uint32_t x = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+        if (lane >= o) incl += x;
+    }
+    if (lane == 31) sm.warp_sum[warp] = incl;
+    __syncthreads();
+    uint32_t wbase = 0, total = 0;
+#pragma unroll
+    for (int w = 0; w < kScanThreads / 32; ++w) {
+        const uint32_t x = sm.warp_sum[w];
+        if (w < warp) wbase += x;
+        total += x;
+    }
+    uint32_t excl = wbase + incl - sum;
+#pragma unroll
+    for (int k = 0; k < kScanPerThread; ++k) {
+        sm.off[tid * kScanPerThread + k] = excl;
+        sm.size[tid * kScanPerThread + k] = v[k];
+        excl += v[k];
+    }
+    if (warp == 0) {
+        if (lane == 0)
+            st_relaxed_u64(&tdesc[t], make_desc(epoch, t == 0 ? kDescInclusive : kDescAggregate,
+                                                total));
+        uint64_t prefix = 0;
+        if (t > 0) {
+            bool to = false;
+            prefix = lookback(tdesc, t, total, epoch, lane, &to);
+            if (to && lane == 0) atomicOr(status, kStatTimeout);
+        }
+        if (lane == 0) {
+            sm.prefix = prefix;
+            sm.total = total;
+        }
+    }
+    __syncthreads();
+    return sm.prefix;
+}
+
 struct EncodeArgs {
     const uint8_t* in;
     uint64_t n_bytes;
     uint8_t* out;
     uint64_t capacity;
     unsigned long long* out_bytes;
-    uint64_t* desc;
+    uint64_t* desc;     // single pass: per chunk aggregate, then inclusive prefix
+    uint8_t* slots;     // two pass: chunk c's block at slots + c * chunk_size
+    uint32_t* sizes;    // two pass: chunk c's block size
+    uint64_t* offsets;  // two pass: chunk c's block offset in the stream
+    uint64_t* tdesc;    // two pass: tile descriptors of the pack pass
+    uint32_t* ticket2;  // two pass: tile ticket of the pack pass
     uint32_t* ticket;
     uint32_t* status;
     uint32_t epoch;
@@ -111,14 +311,18 @@ struct DecodeArgs {
     uint64_t in_bytes;
     uint8_t* out;
     uint64_t n_bytes;
-    uint64_t* desc;
-    uint32_t* ticket;
+    uint64_t* offsets;  // per chunk: stream offset of its block (written by the offset pass)
+    uint64_t* tdesc;    // tile descriptors of the offset pass
+    uint32_t* ticket;   // tile ticket of the offset pass
+    uint32_t* ticket2;  // chunk ticket of the decode pass
     uint32_t* status;
     uint32_t epoch;
 };
 
 // Host launchers (gpulz_encode.cu / gpulz_decode.cu). Return a CUDA error.
-cudaError_t launch_encode(const EncodeArgs& a, int word_size, int match_level,
+// single_pass: one kernel, blocks placed by look-back over chunk descriptors
+// (needs only `desc`); otherwise encode into slots, then the pack pass.
+cudaError_t launch_encode(const EncodeArgs& a, int word_size, int match_level, bool single_pass,
                           cudaStream_t stream);
 cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t stream);
 

@@ -21,7 +21,8 @@ namespace {
 
 using namespace gpulz;
 
-// Largest input the fixed scratch can serve: one 8-byte descriptor per chunk.
+// Largest input the fixed scratch can serve: one 8-byte look-back descriptor
+// per chunk.
 constexpr uint64_t kNoAllocMaxChunks = 65536;
 constexpr size_t kNoAllocHead = 256;  // u32 status at 0, u32 ticket at 4
 constexpr size_t kNoAllocBytes = kNoAllocHead + sizeof(uint64_t) * kNoAllocMaxChunks;
@@ -31,22 +32,35 @@ static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocBytes];
 constexpr int kMaxDevices = 64;
 std::mutex g_mu;
 uint8_t* g_scratch_dev[kMaxDevices] = {};
+uint32_t g_epoch[kMaxDevices] = {};  // last epoch used on each device
 
 // Device address of g_noalloc_scratch on the current device, looked up once
-// per device with that device current.
-cudaError_t scratch_address(uint8_t** out) {
+// per device with that device current, and the next epoch for this call.
+// Look-back entries carry the epoch of the call that wrote them, so only the
+// status word and the ticket have to be cleared per call; when the 16-bit
+// epoch wraps, the whole array is cleared once (*clear_all).
+cudaError_t scratch_address(uint8_t** out, uint32_t* epoch, bool* clear_all) {
     int dev = 0;
     cudaError_t err = cudaGetDevice(&dev);
     if (err != cudaSuccess) return err;
     if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
     std::lock_guard<std::mutex> lock(g_mu);
+    *clear_all = false;
     if (g_scratch_dev[dev] == nullptr) {
         void* p = nullptr;
         err = cudaGetSymbolAddress(&p, g_noalloc_scratch);
         if (err != cudaSuccess) return err;
         g_scratch_dev[dev] = static_cast<uint8_t*>(p);
+        *clear_all = true;
+        g_epoch[dev] = 0;
+    }
+    g_epoch[dev] += 1;
+    if (g_epoch[dev] >= kEpochs) {
+        g_epoch[dev] = 1;
+        *clear_all = true;
     }
     *out = g_scratch_dev[dev];
+    *epoch = g_epoch[dev];
     return cudaSuccess;
 }
 
@@ -71,10 +85,13 @@ extern "C" gpulz_status gpulz_compress_noalloc(const void* d_in, size_t n_bytes,
     const uint64_t chunks = ((uint64_t)n_bytes + chunk_size - 1) / (uint64_t)chunk_size;
     if (chunks > kNoAllocMaxChunks) return GPULZ_ERR_INVALID_ARG;
     uint8_t* base = nullptr;
-    if (scratch_address(&base) != cudaSuccess) return GPULZ_ERR_CUDA;
-    // The array keeps the previous call's contents: clear the status, the
-    // ticket and this call's descriptors, in stream order.
-    if (cudaMemsetAsync(base, 0, kNoAllocHead + sizeof(uint64_t) * chunks, stream) != cudaSuccess)
+    uint32_t epoch = 0;
+    bool clear_all = false;
+    if (scratch_address(&base, &epoch, &clear_all) != cudaSuccess) return GPULZ_ERR_CUDA;
+    // The array keeps the previous call's contents: clear the status word and
+    // the ticket (all of it on first use and when the epoch wraps), in stream
+    // order.
+    if (cudaMemsetAsync(base, 0, clear_all ? kNoAllocBytes : kNoAllocHead, stream) != cudaSuccess)
         return GPULZ_ERR_CUDA;
     EncodeArgs a;
     a.in = static_cast<const uint8_t*>(d_in);
@@ -83,14 +100,20 @@ extern "C" gpulz_status gpulz_compress_noalloc(const void* d_in, size_t n_bytes,
     a.capacity = capacity;
     a.out_bytes = reinterpret_cast<unsigned long long*>(d_out_bytes);
     a.desc = reinterpret_cast<uint64_t*>(base + kNoAllocHead);
+    a.slots = nullptr;
+    a.sizes = nullptr;
+    a.offsets = nullptr;
+    a.tdesc = nullptr;
+    a.ticket2 = nullptr;
     a.ticket = reinterpret_cast<uint32_t*>(base + 4);
     a.status = reinterpret_cast<uint32_t*>(base);
-    a.epoch = 1;
+    a.epoch = epoch;
     a.chunk_size = (uint32_t)chunk_size;
     a.elems = (uint32_t)(chunk_size / word_size);
     a.n_chunks = (uint32_t)chunks;
     a.hash_bits = log2_exact(2u * a.elems);
-    if (launch_encode(a, word_size, match_level, stream) != cudaSuccess) return GPULZ_ERR_CUDA;
+    if (launch_encode(a, word_size, match_level, true, stream) != cudaSuccess)
+        return GPULZ_ERR_CUDA;
     noalloc_report<<<1, 32, 0, stream>>>(a.status, a.out_bytes);
     if (cudaGetLastError() != cudaSuccess) return GPULZ_ERR_CUDA;
     return GPULZ_OK;
