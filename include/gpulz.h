@@ -31,10 +31,13 @@
  * 4096} (elements per chunk = chunk_size / word_size, a power of two >= 256).
  *
  * Memory: every d_* pointer is device memory owned by the caller. The library
- * owns only a small per-(device, stream) scratch area (look-back descriptors,
- * 8 bytes per chunk, ticket counters and a status word). The first call on a
- * stream, or a call with more chunks than any earlier call on it, allocates
- * that scratch (stream-ordered); later calls allocate nothing.
+ * owns one scratch area per (device, stream): a status word, ticket counters,
+ * 12 bytes per chunk (block sizes and offsets) and, for gpulz_compress, one
+ * chunk_size slot per chunk in which each chunk's block is staged before it
+ * is placed (so about n_bytes of scratch for an n_bytes input). The first
+ * call on a stream, or a call needing more room than any earlier call on it,
+ * allocates that scratch stream-ordered (cudaMallocAsync); later calls
+ * allocate nothing. gpulz_compress_noalloc never allocates.
  *
  * Errors: argument errors a host can check are returned synchronously and
  * nothing is launched. Conditions found on the device (corrupt stream, size
