@@ -337,35 +337,67 @@ __global__ void __launch_bounds__(256, 4) encode_kernel(EncodeArgs a) {
                 __syncthreads();
 
                 // ---- E5: level-1 hashed candidates over 8 sub-blocks ----
+                // The sub-block phases only look the buckets up and insert;
+                // the candidates are checked afterwards, with no barrier in
+                // between. Bucket and candidate offset of each position live
+                // in the omask area (the masks are dead once E4 is done).
+                // Sub-block 0 finds an empty table and the last sub-block's
+                // inserts are never looked up, so neither is done. A candidate
+                // at offset d <= 32 never wins: the near search already found
+                // the longest run over offsets 1..32 with the same caps,
+                // nearest first. For d > 32 it wins only with a run longer
+                // than the near length l0, so element l0 is compared first.
                 if (LEVEL) {
+                    uint16_t* s_hk = reinterpret_cast<uint16_t*>(s_om);
+                    uint8_t* s_cd = reinterpret_cast<uint8_t*>(s_om) + 2u * E;
                     const uint32_t SB = E / kSubBlocks;
                     for (int s = 0; s < kSubBlocks; ++s) {
                         const uint32_t lo_i = (uint32_t)s * SB;
                         for (uint32_t i = lo_i + tid; i < lo_i + SB; i += nthreads) {
-                            if (i + 1u >= E) continue;
-                            const uint32_t slot = s_tab[key_hash(el_get<WS>(s_el, i),
-                                                                 el_get<WS>(s_el, i + 1u), a.hash_bits)];
-                            if (!slot) continue;
-                            const uint32_t p = slot - 1u;
-                            const uint32_t d = i - p;
-                            if (d > (uint32_t)kMaxOff) continue;
-                            const uint32_t cap = E - i < (uint32_t)kMaxLen ? E - i : (uint32_t)kMaxLen;
-                            uint32_t k = 0;
-                            while (k < cap && el_get<WS>(s_el, i + k) == el_get<WS>(s_el, p + k)) ++k;
-                            if (!k) continue;
-                            const uint32_t cur = s_lo[i];
-                            const uint32_t l0 = cur & 0xFFu, o0 = cur >> 8;
-                            if (k > l0 || (k == l0 && d < o0)) s_lo[i] = (uint16_t)(k | (d << 8));
+                            uint32_t d = 0;
+                            if (i + 1u < E) {
+                                const uint32_t h =
+                                    key_hash(el_get<WS>(s_el, i), el_get<WS>(s_el, i + 1u), a.hash_bits);
+                                s_hk[i] = (uint16_t)h;
+                                if (s > 0) {
+                                    const uint32_t slot = s_tab[h];
+                                    d = i + 1u - slot;  // i - p for p = slot - 1
+                                    if (slot == 0u || d <= 32u || d > (uint32_t)kMaxOff) d = 0;
+                                }
+                            }
+                            s_cd[i] = (uint8_t)d;
                         }
                         __syncthreads();
-                        for (uint32_t p = lo_i + tid; p < lo_i + SB; p += nthreads) {
-                            if (p + 1u >= E) continue;
-                            atomicMax(&s_tab[key_hash(el_get<WS>(s_el, p), el_get<WS>(s_el, p + 1u),
-                                                      a.hash_bits)],
-                                      p + 1u);
+                        if (s + 1 < kSubBlocks) {
+                            for (uint32_t p = lo_i + tid; p < lo_i + SB; p += nthreads)
+                                if (p + 1u < E) atomicMax(&s_tab[s_hk[p]], p + 1u);
+                            __syncthreads();
                         }
-                        __syncthreads();
                     }
+                    for (uint32_t i = SB + tid; i < E; i += nthreads) {
+                        const uint32_t d = s_cd[i];
+                        if (!d) continue;
+                        const uint32_t p = i - d;
+                        const uint32_t cap = E - i < (uint32_t)kMaxLen ? E - i : (uint32_t)kMaxLen;
+                        const uint32_t l0 = s_lo[i] & 0xFFu;
+                        if (l0 >= cap || el_get<WS>(s_el, i + l0) != el_get<WS>(s_el, p + l0)) continue;
+                        // run length from 0, four element pairs per round
+                        uint32_t k = 0;
+                        for (;;) {
+                            uint32_t eq = 0;
+#pragma unroll
+                            for (int r = 0; r < 4; ++r) {
+                                const uint32_t q = k + (uint32_t)r < cap ? k + (uint32_t)r : cap - 1u;
+                                eq |= (uint32_t)(el_get<WS>(s_el, i + q) == el_get<WS>(s_el, p + q)) << r;
+                            }
+                            const uint32_t lead = (uint32_t)__ffs(~eq) - 1u;  // 0..4
+                            k += lead;
+                            if (lead < 4u || k >= cap) break;
+                        }
+                        if (k > cap) k = cap;
+                        if (k > l0) s_lo[i] = (uint16_t)(k | (d << 8));
+                    }
+                    __syncthreads();
                 }
 
                 // ---- E6: greedy parse, one SEGP-position segment per thread ----

@@ -303,3 +303,25 @@ def test_oracle_decoder_rejects_corruption(orc):
     bad = s.copy()
     bad[32 + 4] ^= 0x40                                        # data_bytes of chunk 0
     assert orc.decompress_status(bad, x.size) != 0
+
+
+def test_level1_changes_only_to_far_and_longer(orc):
+    """The near search is exact over offsets 1..32 with the same caps (255 and
+    the chunk end) and nearest-offset ties, so a hashed candidate can replace
+    the level-0 result only with an offset above 32 and a strictly longer run.
+    Checked on inputs with many near and far repeats."""
+    rng = np.random.default_rng(23)
+    changed = 0
+    for E in (256, 512, 1024, 4096):
+        for alphabet in (2, 3, 8, 64):
+            base = rng.integers(0, alphabet, 48).astype(np.uint32)
+            w = np.tile(base, E // 48 + 1)[:E].copy()
+            flip = rng.random(E) < 0.05
+            w[flip] = rng.integers(0, alphabet, int(flip.sum()))
+            L0, O0 = orc.near_matches(w)
+            L1, O1 = orc.level1_matches(w)
+            diff = (L1 != L0) | (O1 != O0)
+            changed += int(diff.sum())
+            assert (O1[diff] > 32).all()
+            assert (L1[diff] > L0[diff]).all()
+    assert changed > 0
