@@ -1,8 +1,9 @@
 // GPULZ encode kernel for sm_103a.
 //
 // One CTA ("team" of 1..8 warps) codes one chunk at a time and loops over
-// chunks in ticket order (persistent grid). Per chunk, following the GPULZ
-// stage page of FZGPUModules:
+// chunks by ticket (persistent grid); every thread owns a segment of 8
+// consecutive positions (16 for 4096-element chunks). Per chunk, following
+// the GPULZ stage page of FZGPUModules:
 //   E1 load + zero pad         (class summary; "Alignment" paragraph)
 //   E2 zero test -> {0,0}      (zero-chunk paragraph)
 //   E3 near equality masks     (match-search section: bit o-1 of omask[i])
@@ -13,15 +14,15 @@
 //   E7 flag bitmap + packing   (class summary: scan of item sizes, staging
 //                               buffer, coalesced 32-bit stores)
 //   E8 raw fallback            (raw-fallback paragraph)
-//   E9 cross-chunk offsets     (single-pass decoupled look-back, bounded)
+//   E9 cross-chunk offsets     (two pass: tile scan of the block sizes;
+//                               single pass: bounded decoupled look-back)
 //   E10 store-out, size table, header and the stream length
 //
-// The greedy parse is computed in parallel: a warp walks 32-position windows,
-// finding the on-path positions of each window from its first position by
-// pointer doubling over next(i) = i + step(i) with warp reductions. With more
-// than one warp, each warp walks its own segment from the segment start and
-// warp 0 then repairs each segment from its true entry until the repaired
-// path merges with the speculative one (paths that meet coincide afterwards).
+// The greedy parse is computed in parallel: each thread walks its own
+// segment from the segment start, then every thread whose true entry (the
+// previous segment's exit) differs re-walks from it until its path meets the
+// old one (paths that meet coincide afterwards); this repeats until no entry
+// changes, which gives exactly the sequential parse.
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -52,7 +53,11 @@ __host__ __device__ inline EncLayout enc_layout(uint32_t cs, uint32_t E, int lev
     return L;
 }
 
-__host__ __device__ inline int team_warps(uint32_t E) { return E <= 512u ? 1 : (int)(E / 512u); }
+// Warps per chunk: 8-position segments (16 for 4096-element chunks, which
+// would need 16 warps). Short segments keep the register AND-chain triangle
+// small, and more warps per chunk shorten the time a chunk takes, which is
+// what the tail of the persistent grid waits for.
+__host__ __device__ inline int team_warps(uint32_t E) { return E <= 256u ? 1 : (E >= 2048u ? 8 : (int)(E / 256u)); }
 
 // Byte address of element i in the padded element array.
 template <int WS>
@@ -699,7 +704,7 @@ cudaError_t launch_t(const EncodeArgs& a, cudaStream_t stream) {
     static thread_local LaunchShape shape16, shape8, shape_copy;
     const EncLayout L = enc_layout(a.chunk_size, a.elems, LEVEL);
     const int threads = 32 * team_warps(a.elems);
-    // positions per thread: 16, except 8 for 256-element chunks
+    // positions per thread: 8, except 16 for 4096-element chunks
     const bool s16 = a.elems / (uint32_t)threads == 16u;
     auto kern = s16 ? encode_kernel<WS, LEVEL, 16, SINGLE> : encode_kernel<WS, LEVEL, 8, SINGLE>;
     LaunchShape& shape = s16 ? shape16 : shape8;
