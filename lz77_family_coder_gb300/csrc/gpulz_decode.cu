@@ -9,10 +9,9 @@
 // rounds, stopping early once nothing changes. Zero chunks are zero-filled
 // (zero-chunk paragraph) and raw chunks copied (raw-fallback paragraph).
 //
-// Each warp decodes one chunk at a time, in ticket order, so that a warp's
-// stream offset is the sum of the earlier chunks' block sizes. Those sizes are
-// in the size table, so the look-back never waits: where an earlier chunk has
-// not published its inclusive offset yet, its table entry is read instead.
+// A first kernel (offsets_kernel) scans the size table into every chunk's
+// block offset; then each warp of decode_kernel decodes one chunk at a time,
+// taking chunks by ticket.
 //
 // The header is parsed on the device; chunk geometry is not known to the host
 // launcher, so the shared-memory slot per warp is sized from the header at run
@@ -26,7 +25,7 @@ namespace gpulz {
 namespace {
 
 constexpr uint32_t FULL = 0xFFFFFFFFu;
-constexpr int kDecWarps = 8;
+constexpr int kDecWarps = 16;
 constexpr uint32_t kDecSmem = 48u * 1024u;
 constexpr int kMaxJumpRounds = 16;
 constexpr uint16_t kLit = 0x8000u;
@@ -153,13 +152,25 @@ __device__ void decode_chunks(const DecodeArgs& a, const Geo& g, uint8_t* slot_b
         // ---- D2: load flags and items into shared memory ----
         const uint32_t fw = (items + 31u) / 32u;
         const uint32_t dw = (dbytes + 3u) / 4u;
-        for (uint32_t j = lane; j < fw + dw; j += 32) {
-            uint32_t v = read_u32(src + 4u * j);
-            if (j < fw) {
-                if (j == fw - 1u && (items & 31u)) v &= (1u << (items & 31u)) - 1u;
-                s_fl[j] = v;
-            } else {
-                *reinterpret_cast<uint32_t*>(s_data + 4u * (j - fw)) = v;
+        // four loads in flight per lane
+        for (uint32_t j0 = lane; j0 < fw + dw; j0 += 128) {
+            uint32_t vv[4];
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const uint32_t j = j0 + 32u * u;
+                vv[u] = j < fw + dw ? read_u32(src + 4u * j) : 0u;
+            }
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const uint32_t j = j0 + 32u * u;
+                if (j >= fw + dw) break;
+                uint32_t v = vv[u];
+                if (j < fw) {
+                    if (j == fw - 1u && (items & 31u)) v &= (1u << (items & 31u)) - 1u;
+                    s_fl[j] = v;
+                } else {
+                    *reinterpret_cast<uint32_t*>(s_data + 4u * (j - fw)) = v;
+                }
             }
         }
         __syncwarp();
