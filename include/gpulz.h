@@ -155,6 +155,20 @@ gpulz_status gpulz_compress_noalloc(const void* d_in, size_t n_bytes, int word_s
                                     int chunk_size, int match_level, void* d_out,
                                     size_t capacity, size_t* d_out_bytes, cudaStream_t stream);
 
+/*
+ * gpulz_set_kernel_events -- measurement hook (no counterpart in the paper).
+ *
+ * gpulz_compress runs three kernels (encode, tile scan of block sizes, copy to
+ * the stream) and gpulz_decompress two (offset scan, decode). To time the
+ * main one alone, pass two CUDA events (created by the caller, which keeps
+ * ownership): while they are set, every following gpulz_compress and
+ * gpulz_decompress issued from this host thread records `start` on its stream
+ * right before its encode or decode kernel and `stop` right after it. Passing
+ * two nulls clears the hook. Returns GPULZ_ERR_INVALID_ARG if exactly one of
+ * the two is null. The events add no synchronisation.
+ */
+gpulz_status gpulz_set_kernel_events(cudaEvent_t start, cudaEvent_t stop);
+
 /* Static, human-readable name of a status code. */
 const char* gpulz_status_string(gpulz_status status);
 

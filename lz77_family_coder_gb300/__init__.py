@@ -19,7 +19,8 @@ __all__ = [
     "GPULZ_ERR_TIMEOUT", "GPULZ_ERR_CUDA", "GPULZ_ERR_SIZE_MISMATCH", "GpulzError",
     "library_path", "load", "build", "gpulz_compress", "gpulz_compress_noalloc", "gpulz_decompress",
     "gpulz_decompress_bounded", "gpulz_compress_bound", "gpulz_stream_info",
-    "gpulz_device_status", "gpulz_status_string", "compress", "decompress",
+    "gpulz_device_status", "gpulz_set_kernel_events", "gpulz_status_string", "compress",
+    "decompress",
 ]
 
 GPULZ_OK = 0
@@ -75,6 +76,8 @@ def load():
     lib.gpulz_stream_info.restype = i32
     lib.gpulz_device_status.argtypes = [vp]
     lib.gpulz_device_status.restype = i32
+    lib.gpulz_set_kernel_events.argtypes = [vp, vp]
+    lib.gpulz_set_kernel_events.restype = i32
     lib.gpulz_status_string.argtypes = [i32]
     lib.gpulz_status_string.restype = ctypes.c_char_p
     _lib = lib
@@ -146,6 +149,17 @@ def gpulz_stream_info(h_header: bytes):
 
 def gpulz_device_status(stream=None) -> int:
     return load().gpulz_device_status(_stream(stream))
+
+
+def gpulz_set_kernel_events(start, stop) -> int:
+    """Measurement hook: bracket the encode/decode kernel of the following calls
+    from this thread with two CUDA events (torch.cuda.Event, raw handles or
+    None to clear)."""
+    def handle(e):
+        if e is None or isinstance(e, int):
+            return e
+        return e.cuda_event
+    return load().gpulz_set_kernel_events(handle(start), handle(stop))
 
 
 def gpulz_status_string(status: int) -> str:

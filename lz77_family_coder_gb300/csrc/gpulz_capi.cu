@@ -105,6 +105,13 @@ inline bool aligned(const void* p, uintptr_t a) {
 
 }  // namespace
 
+namespace gpulz {
+KernelEvents& kernel_events() {
+    static thread_local KernelEvents ev{nullptr, nullptr};
+    return ev;
+}
+}  // namespace gpulz
+
 extern "C" {
 
 size_t gpulz_compress_bound(size_t n_bytes, int word_size, int chunk_size) {
@@ -220,6 +227,12 @@ gpulz_status gpulz_device_status(cudaStream_t stream) {
     if (bits & kStatSizeMismatch) return GPULZ_ERR_SIZE_MISMATCH;
     if (bits & kStatTimeout) return GPULZ_ERR_TIMEOUT;
     if (bits & kStatCapacity) return GPULZ_ERR_CAPACITY;
+    return GPULZ_OK;
+}
+
+gpulz_status gpulz_set_kernel_events(cudaEvent_t start, cudaEvent_t stop) {
+    if ((start == nullptr) != (stop == nullptr)) return GPULZ_ERR_INVALID_ARG;
+    kernel_events() = KernelEvents{start, stop};
     return GPULZ_OK;
 }
 

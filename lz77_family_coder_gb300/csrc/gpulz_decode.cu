@@ -315,6 +315,7 @@ __device__ bool parse_header(const DecodeArgs& a, Geo& g) {
 // ---- D1: stream offset of every chunk's block (scan of the size table) ----
 __global__ void __launch_bounds__(kScanThreads) offsets_kernel(DecodeArgs a) {
     __shared__ TileSmem sm;
+    pdl_trigger();  // the decode kernel may be scheduled now
     Geo g;
     if (!parse_header(a, g)) return;
     const int tid = threadIdx.x;
@@ -343,6 +344,7 @@ __global__ void __launch_bounds__(kDecWarps * 32) decode_kernel(DecodeArgs a) {
     extern __shared__ __align__(16) uint8_t smem[];
     const int lane = threadIdx.x & 31;
     const int warp = threadIdx.x >> 5;
+    pdl_wait();  // the block offsets
     Geo g;
     if (!parse_header(a, g)) return;
     const DecSlot S = dec_slot(g.cs, g.E);
@@ -393,8 +395,13 @@ cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t stream) {
     uint64_t grid = (uint64_t)grid_cache;
     if (grid > max_ctas) grid = max_ctas;
     if (grid < 1) grid = 1;
-    decode_kernel<<<(unsigned)grid, kDecWarps * 32, kDecSmem, stream>>>(a);
-    return cudaGetLastError();
+    const KernelEvents ev = kernel_events();
+    if (ev.start && (err = cudaEventRecord(ev.start, stream)) != cudaSuccess) return err;
+    if ((err = pdl_launch(decode_kernel, dim3((unsigned)grid), dim3(kDecWarps * 32), kDecSmem, stream, a)) !=
+        cudaSuccess)
+        return err;
+    if (ev.stop && (err = cudaEventRecord(ev.stop, stream)) != cudaSuccess) return err;
+    return cudaSuccess;
 }
 
 }  // namespace gpulz

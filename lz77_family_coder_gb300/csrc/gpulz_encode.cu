@@ -198,6 +198,7 @@ __global__ void __launch_bounds__(256, 4) encode_kernel(EncodeArgs a) {
     constexpr uint32_t LMIN = (uint32_t)min_match_len(WS);
     constexpr uint32_t NONE = 0xFFFFFFFFu;
 
+    if (!SINGLE) pdl_trigger();  // the pack pass may be scheduled as CTAs retire
     if (a.n_chunks == 0) {
         if (blockIdx.x == 0 && tid == 0) write_header(a, WS, kHeaderBytes);
         return;
@@ -628,6 +629,8 @@ __global__ void __launch_bounds__(256, 4) encode_kernel(EncodeArgs a) {
 __global__ void __launch_bounds__(kScanThreads) offsets_pass(EncodeArgs a, uint32_t ws) {
     __shared__ TileSmem sm;
     const int tid = threadIdx.x;
+    pdl_trigger();
+    pdl_wait();  // the encode kernel's sizes
     const uint32_t n_tiles = (a.n_chunks + kTile - 1) / kTile;
     if (a.n_chunks == 0) {
         if (blockIdx.x == 0 && tid == 0) write_header(a, ws, kHeaderBytes);
@@ -653,6 +656,7 @@ constexpr int kCopyWarps = 8;
 
 __global__ void __launch_bounds__(kCopyWarps * 32) copy_pass(EncodeArgs a) {
     const int lane = threadIdx.x & 31;
+    pdl_wait();  // the offsets (and, through them, the slots)
     const uint32_t gw = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
     const uint32_t nw = (gridDim.x * blockDim.x) >> 5;
     for (uint32_t c = gw; c < a.n_chunks; c += nw) {
@@ -713,23 +717,26 @@ cudaError_t launch_t(const EncodeArgs& a, cudaStream_t stream) {
     uint64_t grid = (uint64_t)shape.sms * (uint64_t)shape.per_sm;
     if (grid > a.n_chunks) grid = a.n_chunks;
     if (grid < 1) grid = 1;
+    const KernelEvents ev = SINGLE ? KernelEvents{nullptr, nullptr} : kernel_events();
+    if (ev.start && (err = cudaEventRecord(ev.start, stream)) != cudaSuccess) return err;
     kern<<<(unsigned)grid, threads, L.total, stream>>>(a);
     if ((err = cudaGetLastError()) != cudaSuccess) return err;
+    if (ev.stop && (err = cudaEventRecord(ev.stop, stream)) != cudaSuccess) return err;
     if (!SINGLE) {
         const uint64_t tiles = (a.n_chunks + kTile - 1) / kTile;
         uint64_t sgrid = (uint64_t)shape.sms * 4u;
         if (sgrid > tiles) sgrid = tiles;
         if (sgrid < 1) sgrid = 1;
-        offsets_pass<<<(unsigned)sgrid, kScanThreads, 0, stream>>>(a, (uint32_t)WS);
-        if ((err = cudaGetLastError()) != cudaSuccess) return err;
+        if ((err = pdl_launch(offsets_pass, dim3((unsigned)sgrid), dim3(kScanThreads), 0, stream, a,
+                              (uint32_t)WS)) != cudaSuccess)
+            return err;
         if (a.n_chunks > 0) {
             if ((err = shape_for(copy_pass, kCopyWarps * 32, 0, shape_copy)) != cudaSuccess)
                 return err;
             uint64_t cgrid = (uint64_t)shape_copy.sms * (uint64_t)shape_copy.per_sm;
             const uint64_t need = (a.n_chunks + kCopyWarps - 1) / kCopyWarps;
             if (cgrid > need) cgrid = need;
-            copy_pass<<<(unsigned)cgrid, kCopyWarps * 32, 0, stream>>>(a);
-            err = cudaGetLastError();
+            err = pdl_launch(copy_pass, dim3((unsigned)cgrid), dim3(kCopyWarps * 32), 0, stream, a);
         }
     }
     return err;

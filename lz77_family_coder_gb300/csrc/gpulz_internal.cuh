@@ -319,6 +319,36 @@ struct DecodeArgs {
     uint32_t epoch;
 };
 
+// Programmatic dependent launch: a kernel launched with pdl_launch() may be
+// scheduled before the previous kernel in the stream has finished; it calls
+// pdl_wait() before it reads anything that kernel writes (the wait returns
+// once that kernel has completed and its memory is visible). pdl_trigger()
+// lets the next kernel be scheduled early.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+template <typename... KArgs, typename... Args>
+cudaError_t pdl_launch(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
+                       Args... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, args...);
+}
+
+// Events a caller asked to bracket the main kernel with (see
+// gpulz_set_kernel_events); both null when unset. Per host thread.
+struct KernelEvents {
+    cudaEvent_t start, stop;
+};
+KernelEvents& kernel_events();
+
 // Host launchers (gpulz_encode.cu / gpulz_decode.cu). Return a CUDA error.
 // single_pass: one kernel, blocks placed by look-back over chunk descriptors
 // (needs only `desc`); otherwise encode into slots, then the pack pass.

@@ -69,3 +69,10 @@ def test_invalid_arguments_rejected_before_any_launch(g):
 def test_status_strings(g):
     for code in range(7):
         assert g.gpulz_status_string(code)
+
+
+def test_kernel_events_hook_arguments(g):
+    """Both events or neither: a half-set hook is refused, clearing is fine."""
+    assert g.gpulz_set_kernel_events(1 << 20, None) == g.GPULZ_ERR_INVALID_ARG
+    assert g.gpulz_set_kernel_events(None, 1 << 20) == g.GPULZ_ERR_INVALID_ARG
+    assert g.gpulz_set_kernel_events(None, None) == g.GPULZ_OK
