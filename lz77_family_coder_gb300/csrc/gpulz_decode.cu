@@ -25,8 +25,8 @@ namespace gpulz {
 namespace {
 
 constexpr uint32_t FULL = 0xFFFFFFFFu;
-constexpr int kDecWarps = 16;
-constexpr uint32_t kDecSmem = 48u * 1024u;
+constexpr int kDecWarps = 24;
+constexpr uint32_t kDecSmem = 112u * 1024u;
 constexpr int kMaxJumpRounds = 16;
 constexpr uint16_t kLit = 0x8000u;
 
