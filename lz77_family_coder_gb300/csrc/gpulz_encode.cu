@@ -71,6 +71,19 @@ __device__ __forceinline__ uint32_t el_get(const uint8_t* el, uint32_t i) {
     if (WS == 2) return *reinterpret_cast<const uint16_t*>(p);
     return *p;
 }
+// Element i of an unpadded element array (level 1 keeps one in the staging
+// buffer while the match search runs).
+template <int WS>
+__device__ __forceinline__ uint32_t lin_get(const uint8_t* lin, uint32_t i) {
+    if (WS == 4) return reinterpret_cast<const uint32_t*>(lin)[i];
+    if (WS == 2) return reinterpret_cast<const uint16_t*>(lin)[i];
+    return lin[i];
+}
+template <int WS>
+__device__ __forceinline__ uint32_t lin_at(const uint8_t* p, uint32_t k) {
+    return lin_get<WS>(p, k);
+}
+
 // Word index of omask[i] in the padded omask array.
 __device__ __forceinline__ uint32_t om_idx(uint32_t i) { return i + ((i >> 4) << 2); }
 
@@ -236,6 +249,7 @@ __global__ void __launch_bounds__(256, 4) encode_kernel(EncodeArgs a) {
                     const uint4 v = __ldg(src + g);
                     uint32_t* dst = reinterpret_cast<uint32_t*>(s_el + chunk_byte_addr<WS>(16u * g));
                     dst[0] = v.x; dst[1] = v.y; dst[2] = v.z; dst[3] = v.w;
+                    if (LEVEL && !SINGLE) reinterpret_cast<uint4*>(s_data)[g] = v;
                     nz |= v.x | v.y | v.z | v.w;
                 }
             } else {
@@ -246,6 +260,7 @@ __global__ void __launch_bounds__(256, 4) encode_kernel(EncodeArgs a) {
                         if (b < take) v |= (uint32_t)a.in[begin + b] << (8u * k);
                     }
                     *reinterpret_cast<uint32_t*>(s_el + chunk_byte_addr<WS>(4u * b4)) = v;
+                    if (LEVEL && !SINGLE) reinterpret_cast<uint32_t*>(s_data)[b4] = v;
                     nz |= v;
                 }
             }
@@ -352,7 +367,9 @@ __global__ void __launch_bounds__(256, 4) encode_kernel(EncodeArgs a) {
                 // at offset d <= 32 never wins: the near search already found
                 // the longest run over offsets 1..32 with the same caps,
                 // nearest first. For d > 32 it wins only with a run longer
-                // than the near length l0, so element l0 is compared first.
+                // than the near length l0. In the two-pass kernel the staging
+                // buffer is idle until E7 and holds an unpadded copy of the
+                // chunk (written in E1) for the hashing and the compares.
                 if (LEVEL) {
                     uint16_t* s_hk = reinterpret_cast<uint16_t*>(s_om);
                     uint8_t* s_cd = reinterpret_cast<uint8_t*>(s_om) + 2u * E;
@@ -363,7 +380,8 @@ __global__ void __launch_bounds__(256, 4) encode_kernel(EncodeArgs a) {
                             uint32_t d = 0;
                             if (i + 1u < E) {
                                 const uint32_t h =
-                                    key_hash(el_get<WS>(s_el, i), el_get<WS>(s_el, i + 1u), a.hash_bits);
+                                    SINGLE ? key_hash(el_get<WS>(s_el, i), el_get<WS>(s_el, i + 1u), a.hash_bits)
+                                           : key_hash(lin_get<WS>(s_data, i), lin_get<WS>(s_data, i + 1u), a.hash_bits);
                                 s_hk[i] = (uint16_t)h;
                                 if (s > 0) {
                                     const uint32_t slot = s_tab[h];
@@ -383,22 +401,43 @@ __global__ void __launch_bounds__(256, 4) encode_kernel(EncodeArgs a) {
                     for (uint32_t i = SB + tid; i < E; i += nthreads) {
                         const uint32_t d = s_cd[i];
                         if (!d) continue;
-                        const uint32_t p = i - d;
                         const uint32_t cap = E - i < (uint32_t)kMaxLen ? E - i : (uint32_t)kMaxLen;
                         const uint32_t l0 = s_lo[i] & 0xFFu;
-                        if (l0 >= cap || el_get<WS>(s_el, i + l0) != el_get<WS>(s_el, p + l0)) continue;
-                        // run length from 0, four element pairs per round
+                        if (l0 >= cap) continue;
                         uint32_t k = 0;
-                        for (;;) {
-                            uint32_t eq = 0;
+                        if constexpr (!SINGLE) {
+                            // run length from 0, four element pairs per round,
+                            // from the unpadded copy in the staging buffer:
+                            // reads past the cap (at most 3 elements past the
+                            // chunk, inside the buffer's 16 spare bytes) can only
+                            // lengthen the run, which the cap then cuts
+                            const uint8_t* pa = s_data + i * WS;
+                            const uint8_t* pb = pa - d * WS;
+                            for (;;) {
+                                uint32_t eq = 0;
 #pragma unroll
-                            for (int r = 0; r < 4; ++r) {
-                                const uint32_t q = k + (uint32_t)r < cap ? k + (uint32_t)r : cap - 1u;
-                                eq |= (uint32_t)(el_get<WS>(s_el, i + q) == el_get<WS>(s_el, p + q)) << r;
+                                for (int r = 0; r < 4; ++r)
+                                    eq |= (uint32_t)(lin_at<WS>(pa, k + (uint32_t)r) == lin_at<WS>(pb, k + (uint32_t)r)) << r;
+                                const uint32_t lead = (uint32_t)__ffs(~eq) - 1u;  // 0..4
+                                k += lead;
+                                if (lead < 4u || k >= cap) break;
                             }
-                            const uint32_t lead = (uint32_t)__ffs(~eq) - 1u;  // 0..4
-                            k += lead;
-                            if (lead < 4u || k >= cap) break;
+                        } else {
+                            // the staging buffer holds the previous chunk's block
+                            // here: compare in the padded element array
+                            const uint32_t p = i - d;
+                            if (el_get<WS>(s_el, i + l0) != el_get<WS>(s_el, p + l0)) continue;
+                            for (;;) {
+                                uint32_t eq = 0;
+#pragma unroll
+                                for (int r = 0; r < 4; ++r) {
+                                    const uint32_t q = k + (uint32_t)r < cap ? k + (uint32_t)r : cap - 1u;
+                                    eq |= (uint32_t)(el_get<WS>(s_el, i + q) == el_get<WS>(s_el, p + q)) << r;
+                                }
+                                const uint32_t lead = (uint32_t)__ffs(~eq) - 1u;  // 0..4
+                                k += lead;
+                                if (lead < 4u || k >= cap) break;
+                            }
                         }
                         if (k > cap) k = cap;
                         if (k > l0) s_lo[i] = (uint16_t)(k | (d << 8));
