@@ -107,7 +107,10 @@ __device__ uint32_t lit_word(const uint8_t* s_data, const uint16_t* s_src, uint3
 }
 
 template <int WS>
-__device__ void decode_chunks(const DecodeArgs& a, const Geo& g, uint8_t* slot_base, int lane) {
+// A warp's first chunk is its index among the kernel's decoding warps (no
+// ticket storm at start-up); later chunks come by ticket, after those.
+__device__ void decode_chunks(const DecodeArgs& a, const Geo& g, uint8_t* slot_base, int lane,
+                              uint32_t first, uint32_t n_warps) {
     const DecSlot S = dec_slot(g.cs, g.E);
     uint32_t* s_fl = reinterpret_cast<uint32_t*>(slot_base + S.fl);
     uint32_t* s_wp = reinterpret_cast<uint32_t*>(slot_base + S.wp);
@@ -115,10 +118,12 @@ __device__ void decode_chunks(const DecodeArgs& a, const Geo& g, uint8_t* slot_b
     uint16_t* s_src = reinterpret_cast<uint16_t*>(slot_base + S.src);
     const uint32_t E = g.E, CS = g.cs;
     const bool out_aligned = (reinterpret_cast<uintptr_t>(a.out) & 3u) == 0;
-    for (;;) {
-        uint32_t c = 0;
-        if (lane == 0) c = atomicAdd(a.ticket2, 1u);
-        c = __shfl_sync(FULL, c, 0);
+    for (bool initial = true;; initial = false) {
+        uint32_t c = first;
+        if (!initial) {
+            if (lane == 0) c = atomicAdd(a.ticket2, 1u) + n_warps;
+            c = __shfl_sync(FULL, c, 0);
+        }
         if (c >= g.C) break;
 
         const uint8_t* e = a.in + kHeaderBytes + (uint64_t)kEntryBytes * c;
@@ -351,12 +356,14 @@ __global__ void __launch_bounds__(kDecWarps * 32) decode_kernel(DecodeArgs a) {
     const int slots = (int)(kDecSmem / S.total) < kDecWarps ? (int)(kDecSmem / S.total) : kDecWarps;
     if (warp >= slots) return;
     uint8_t* slot = smem + (size_t)warp * S.total;
+    const uint32_t first = (uint32_t)warp * gridDim.x + blockIdx.x;  // spread over the SMs
+    const uint32_t n_warps = gridDim.x * (uint32_t)slots;
     if (g.ws == 4)
-        decode_chunks<4>(a, g, slot, lane);
+        decode_chunks<4>(a, g, slot, lane, first, n_warps);
     else if (g.ws == 2)
-        decode_chunks<2>(a, g, slot, lane);
+        decode_chunks<2>(a, g, slot, lane, first, n_warps);
     else
-        decode_chunks<1>(a, g, slot, lane);
+        decode_chunks<1>(a, g, slot, lane, first, n_warps);
 }
 
 }  // namespace
