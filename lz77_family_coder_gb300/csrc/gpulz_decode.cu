@@ -256,15 +256,23 @@ __device__ void decode_chunks(const DecodeArgs& a, const Geo& g, uint8_t* slot_b
         __syncwarp();
 
         // ---- D5: pointer jumping ----
+        // Elements in pairs: one 32-bit shared load and store per two.
+        // Entries change only towards their final value, so a concurrent
+        // reader sees an old or a new pointer, and both are valid.
         bool unresolved = true;
+        uint32_t* s_src2 = reinterpret_cast<uint32_t*>(s_src);
         for (int r = 0; r < kMaxJumpRounds && unresolved; ++r) {
             bool mine = false;
-            for (uint32_t i = lane; i < E; i += 32) {
-                uint16_t s = s_src[i];
-                if (!(s & kLit)) {
-                    uint16_t s2 = s_src[s];
-                    s_src[i] = s2;
-                    mine |= !(s2 & kLit);
+#pragma unroll 2
+            for (uint32_t j = lane; j < E / 2u; j += 32) {
+                const uint32_t v = s_src2[j];
+                uint32_t lo = v & 0xFFFFu, hi = v >> 16;
+                const bool rl = !(lo & kLit), rh = !(hi & kLit);
+                if (rl | rh) {
+                    if (rl) lo = s_src[lo];
+                    if (rh) hi = s_src[hi];
+                    s_src2[j] = lo | (hi << 16);
+                    mine |= !(lo & kLit) || !(hi & kLit);
                 }
             }
             unresolved = __any_sync(FULL, mine);
