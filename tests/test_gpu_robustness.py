@@ -154,3 +154,45 @@ def test_dirty_output_memory(orc):
         assert g.gpulz_compress(d, x.size, 4, 2048, 0, out, out.numel(), nb) == g.GPULZ_OK
         assert g.gpulz_device_status() == g.GPULZ_OK
         assert np.array_equal(out[: ref.size].cpu().numpy(), ref)
+
+
+def test_kernel_events_hook_brackets_the_main_kernels(orc):
+    """The measurement hook records the caller's events around the encode and
+    decode kernels: both pairs complete with a positive elapsed time inside
+    the whole call's, the results are unchanged, and clearing the hook stops
+    further records."""
+    import torch
+    g = lib()
+    x = _workload()
+    ref = orc.compress(x, 4, 2048, 0)
+    d_in = to_dev(x)
+    cap = g.gpulz_compress_bound(x.size, 4, 2048)
+    out = torch.empty(cap, dtype=torch.uint8, device="cuda")
+    nb = torch.zeros(1, dtype=torch.int64, device="cuda")
+    y = torch.empty(x.size, dtype=torch.uint8, device="cuda")
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(6)]
+    for e in ev:
+        e.record()  # creates the events
+    torch.cuda.synchronize()
+    ev[0].record()
+    assert g.gpulz_set_kernel_events(ev[1], ev[2]) == g.GPULZ_OK
+    assert g.gpulz_compress(d_in, x.size, 4, 2048, 0, out, cap, nb) == g.GPULZ_OK
+    assert g.gpulz_set_kernel_events(ev[3], ev[4]) == g.GPULZ_OK
+    assert g.gpulz_decompress(out, y, x.size) == g.GPULZ_OK
+    assert g.gpulz_set_kernel_events(None, None) == g.GPULZ_OK
+    ev[5].record()
+    torch.cuda.synchronize()
+    assert g.gpulz_device_status() == g.GPULZ_OK
+    n = int(nb.item())
+    assert np.array_equal(out[:n].cpu().numpy(), ref)
+    assert np.array_equal(y.cpu().numpy(), x)
+    t_enc = ev[1].elapsed_time(ev[2])
+    t_dec = ev[3].elapsed_time(ev[4])
+    t_all = ev[0].elapsed_time(ev[5])
+    assert 0 < t_enc < t_all and 0 < t_dec < t_all
+    assert t_enc + t_dec <= t_all
+    # cleared: a further call leaves the events where they were
+    stamp = ev[1].elapsed_time(ev[2])
+    assert g.gpulz_compress(d_in, x.size, 4, 2048, 0, out, cap, nb) == g.GPULZ_OK
+    torch.cuda.synchronize()
+    assert ev[1].elapsed_time(ev[2]) == stamp
