@@ -86,6 +86,13 @@ def _load():
         lib.orc_decode_chunk_range.argtypes = [u8p, ctypes.c_uint64, u64p, u8p, ctypes.c_uint64,
                                                ctypes.c_uint64, ctypes.c_uint64]
         lib.orc_decode_chunk_range.restype = ctypes.c_int
+        lib.orc_split_bounds.argtypes = [ctypes.c_uint64, ctypes.c_int, ctypes.c_int, u64p]
+        lib.orc_split_bounds.restype = None
+        lib.orc_compress_split.argtypes = [u8p, ctypes.c_uint64, ctypes.c_int, ctypes.c_int,
+                                           ctypes.c_int, u8p, u8p, u8p, u8p, u64p]
+        lib.orc_compress_split.restype = ctypes.c_int
+        lib.orc_decompress_split.argtypes = [u8p, u8p, u8p, u8p, u64p, u8p, ctypes.c_uint64]
+        lib.orc_decompress_split.restype = ctypes.c_int
         _lib = lib
         return lib
 
@@ -168,6 +175,52 @@ def decompress(stream, n_bytes: int) -> np.ndarray:
     if rc != 0:
         raise ValueError("oracle decompress failed with code %d" % rc)
     return out[:n_bytes]
+
+
+PORTS = ("meta", "literals", "lengths", "offsets")
+
+
+def split_bounds(n_bytes: int, word_size: int, chunk_size: int) -> list[int]:
+    """Upper bounds on the four split-mode ports' byte lengths."""
+    b = np.zeros(4, np.uint64)
+    _load().orc_split_bounds(n_bytes, word_size, chunk_size,
+                             b.ctypes.data_as(ctypes.POINTER(ctypes.c_uint64)))
+    return [int(v) for v in b]
+
+
+def compress_split(data, word_size: int, chunk_size: int, match_level: int) -> list[np.ndarray]:
+    """Split-mode encode; returns the four ports (meta, literals, lengths,
+    offsets) as uint8 arrays."""
+    src = _as_bytes(data)
+    bounds = split_bounds(src.size, word_size, chunk_size)
+    ports = [np.zeros(max(b, 1), np.uint8) for b in bounds]
+    sizes = np.zeros(4, np.uint64)
+    rc = _load().orc_compress_split(_u8(src), src.size, word_size, chunk_size, match_level,
+                                    *[_u8(p) for p in ports],
+                                    sizes.ctypes.data_as(ctypes.POINTER(ctypes.c_uint64)))
+    if rc != 0:
+        raise ValueError("oracle split compress failed with code %d" % rc)
+    return [p[:int(n)].copy() for p, n in zip(ports, sizes)]
+
+
+def decompress_split_status(ports, n_bytes: int):
+    """Split-mode decode; returns (status, output)."""
+    ps = [_as_bytes(p) for p in ports]
+    bufs = [p if p.size else np.zeros(1, np.uint8) for p in ps]
+    lens = np.array([p.size for p in ps], np.uint64)
+    out = np.zeros(max(n_bytes, 1), np.uint8)
+    rc = _load().orc_decompress_split(*[_u8(b) for b in bufs],
+                                      lens.ctypes.data_as(ctypes.POINTER(ctypes.c_uint64)),
+                                      _u8(out), n_bytes)
+    return rc, out[:n_bytes]
+
+
+def decompress_split(ports, n_bytes: int) -> np.ndarray:
+    """Split-mode decode; raises ValueError on corrupt ports."""
+    rc, out = decompress_split_status(ports, n_bytes)
+    if rc != 0:
+        raise ValueError("oracle split decompress failed with code %d" % rc)
+    return out
 
 
 def decompress_status(stream, n_bytes: int) -> int:

@@ -486,3 +486,189 @@ int orc_decode_chunk_range(const uint8_t* in, uint64_t in_len, const uint64_t* b
     free(chunk);
     return rc;
 }
+
+/* ------------------------------------------------------------------------ */
+/* Split mode: the same items, laid out as four ports.                      */
+/* ------------------------------------------------------------------------ */
+/* Stage page, split-mode section (and CN-GPULZ-1): instead of one interleaved
+ * stream the coder emits four ports -- literals (literal words back to back;
+ * a raw-fallback chunk lands here whole), lengths (one byte per match token),
+ * offsets (one byte per match token) and meta (stream header, per-chunk size
+ * table and the flag bitmaps). The pages fix the ports' contents, not their
+ * byte layout; the oracle takes this one (the repository's format notes):
+ *
+ *   meta: 48-byte header {u32 magic, u16 version 2, u8 word_size, u8 0,
+ *         u32 chunk_size, u32 n_chunks, u64 orig_bytes, u64 meta_bytes,
+ *         u64 literal_bytes, u64 n_matches}, then n_chunks entries
+ *         {u32 n_items | RAW << 31, u32 n_matches} ({0,0} zero chunk,
+ *         {RAW,0} raw chunk), then every coded chunk's flag words
+ *         (ceil(n_items/32) u32, LSB first, 1 = match) in chunk order;
+ *   literals, lengths, offsets: chunk order, back to back, no padding.
+ *
+ * The items are exactly those of the single-stream form (same parse, same
+ * raw decision): split mode only moves bytes. */
+#define ORC_SPLIT_VERSION 2u
+#define ORC_SPLIT_HEADER_BYTES 48u
+
+void orc_split_bounds(uint64_t n_bytes, int word_size, int chunk_size, uint64_t bounds[4]) {
+    uint64_t chunks = (n_bytes + (uint64_t)chunk_size - 1) / (uint64_t)chunk_size;
+    uint64_t elems = (uint64_t)(chunk_size / word_size);
+    bounds[0] = ORC_SPLIT_HEADER_BYTES + ORC_ENTRY_BYTES * chunks + 4u * chunks * ((elems + 31u) / 32u);
+    bounds[1] = chunks * (uint64_t)chunk_size;
+    bounds[2] = chunks * elems;
+    bounds[3] = chunks * elems;
+}
+
+int orc_compress_split(const uint8_t* in, uint64_t n_bytes, int word_size, int chunk_size,
+                       int match_level, uint8_t* meta, uint8_t* lits, uint8_t* lens,
+                       uint8_t* offs, uint64_t sizes[4]) {
+    if (!orc_valid_geometry(word_size, chunk_size)) return ORC_ERR_INVALID_ARG;
+    if (match_level != 0 && match_level != 1) return ORC_ERR_INVALID_ARG;
+    if (n_bytes > 0 && in == NULL) return ORC_ERR_INVALID_ARG;
+    uint64_t chunks = (n_bytes + (uint64_t)chunk_size - 1) / (uint64_t)chunk_size;
+    if (chunks > 0xFFFFFFFFull) return ORC_ERR_INVALID_ARG;
+    uint8_t* chunk = (uint8_t*)malloc((size_t)chunk_size);
+    uint8_t* block = (uint8_t*)malloc((size_t)chunk_size);
+    uint64_t flag_at = ORC_SPLIT_HEADER_BYTES + ORC_ENTRY_BYTES * chunks;
+    uint64_t nl = 0, nm = 0;
+    for (uint64_t c = 0; c < chunks; ++c) {
+        uint64_t begin = c * (uint64_t)chunk_size;
+        uint64_t take = n_bytes - begin;
+        if (take > (uint64_t)chunk_size) take = (uint64_t)chunk_size;
+        memset(chunk, 0, (size_t)chunk_size);
+        memcpy(chunk, in + begin, (size_t)take);
+        uint32_t items = 0, dbytes = 0;
+        orc_encode_chunk(chunk, word_size, chunk_size, match_level, block, &items, &dbytes);
+        uint8_t* e = meta + ORC_SPLIT_HEADER_BYTES + ORC_ENTRY_BYTES * c;
+        if (items == ORC_RAW_BIT) {
+            memcpy(lits + nl, block, (size_t)chunk_size);
+            nl += (uint64_t)chunk_size;
+            put_u32(e, ORC_RAW_BIT);
+            put_u32(e + 4, 0);
+            continue;
+        }
+        uint32_t fwords = (items + 31u) / 32u;
+        memcpy(meta + flag_at, block, 4u * (size_t)fwords);
+        flag_at += 4u * (uint64_t)fwords;
+        const uint8_t* data = block + 4u * fwords;
+        uint32_t b = 0, m = 0;
+        for (uint32_t j = 0; j < items; ++j) {
+            if ((get_u32(block + 4u * (j / 32u)) >> (j % 32u)) & 1u) {
+                lens[nm + m] = data[b];
+                offs[nm + m] = data[b + 1];
+                b += 2;
+                ++m;
+            } else {
+                memcpy(lits + nl, data + b, (size_t)word_size);
+                nl += (uint64_t)word_size;
+                b += (uint32_t)word_size;
+            }
+        }
+        nm += m;
+        put_u32(e, items);
+        put_u32(e + 4, m);
+    }
+    free(chunk);
+    free(block);
+    put_u32(meta + 0, ORC_MAGIC);
+    put_u16(meta + 4, ORC_SPLIT_VERSION);
+    meta[6] = (uint8_t)word_size;
+    meta[7] = 0;
+    put_u32(meta + 8, (uint32_t)chunk_size);
+    put_u32(meta + 12, (uint32_t)chunks);
+    put_u64(meta + 16, n_bytes);
+    put_u64(meta + 24, flag_at);
+    put_u64(meta + 32, nl);
+    put_u64(meta + 40, nm);
+    sizes[0] = flag_at;
+    sizes[1] = nl;
+    sizes[2] = nm;
+    sizes[3] = nm;
+    return 0;
+}
+
+/* Sequential replay out of the four ports. port_len[k] are the bytes
+ * available in each port. Returns 0, or a negative ORC_ERR_* code. */
+int orc_decompress_split(const uint8_t* meta, const uint8_t* lits, const uint8_t* lens,
+                         const uint8_t* offs, const uint64_t port_len[4], uint8_t* out,
+                         uint64_t n_bytes) {
+    if (port_len[0] < ORC_SPLIT_HEADER_BYTES) return ORC_ERR_CORRUPT;
+    if (get_u32(meta) != ORC_MAGIC || get_u16(meta + 4) != ORC_SPLIT_VERSION || meta[7] != 0)
+        return ORC_ERR_CORRUPT;
+    int ws = meta[6];
+    int cs = (int)get_u32(meta + 8);
+    if (!orc_valid_geometry(ws, cs)) return ORC_ERR_CORRUPT;
+    uint64_t chunks = get_u32(meta + 12), orig = get_u64(meta + 16);
+    uint64_t meta_bytes = get_u64(meta + 24), nlit = get_u64(meta + 32), nmat = get_u64(meta + 40);
+    if (orig != n_bytes || chunks != (orig + (uint64_t)cs - 1) / (uint64_t)cs) return ORC_ERR_CORRUPT;
+    uint64_t flag_at = ORC_SPLIT_HEADER_BYTES + ORC_ENTRY_BYTES * chunks;
+    if (meta_bytes < flag_at || meta_bytes > port_len[0] || nlit > port_len[1] ||
+        nmat > port_len[2] || nmat > port_len[3])
+        return ORC_ERR_CORRUPT;
+    int elems = cs / ws;
+    uint8_t* chunk = (uint8_t*)malloc((size_t)cs);
+    uint64_t li = 0, mi = 0;
+    int rc = 0;
+    for (uint64_t c = 0; c < chunks && rc == 0; ++c) {
+        const uint8_t* e = meta + ORC_SPLIT_HEADER_BYTES + ORC_ENTRY_BYTES * c;
+        uint32_t items = get_u32(e), m = get_u32(e + 4);
+        if (items == 0 && m == 0) {
+            memset(chunk, 0, (size_t)cs);
+        } else if (items == ORC_RAW_BIT && m == 0) {
+            if (li + (uint64_t)cs > nlit) {
+                rc = ORC_ERR_CORRUPT;
+                break;
+            }
+            memcpy(chunk, lits + li, (size_t)cs);
+            li += (uint64_t)cs;
+        } else if ((items & ORC_RAW_BIT) || items == 0 || items > (uint32_t)elems) {
+            rc = ORC_ERR_CORRUPT;
+            break;
+        } else {
+            uint32_t fwords = (items + 31u) / 32u;
+            if (flag_at + 4u * (uint64_t)fwords > meta_bytes) {
+                rc = ORC_ERR_CORRUPT;
+                break;
+            }
+            const uint8_t* fl = meta + flag_at;
+            flag_at += 4u * (uint64_t)fwords;
+            int q = 0;
+            uint32_t seen = 0;
+            for (uint32_t j = 0; j < items && rc == 0; ++j) {
+                if ((get_u32(fl + 4u * (j / 32u)) >> (j % 32u)) & 1u) {
+                    if (mi >= nmat || seen >= m) {
+                        rc = ORC_ERR_CORRUPT;
+                        break;
+                    }
+                    int L = lens[mi], O = offs[mi];
+                    ++mi;
+                    ++seen;
+                    if (L < 1 || O < 1 || O > q || q + L > elems) {
+                        rc = ORC_ERR_CORRUPT;
+                        break;
+                    }
+                    for (int k = 0; k < L; ++k)
+                        memcpy(chunk + (size_t)(q + k) * ws, chunk + (size_t)(q + k - O) * ws, (size_t)ws);
+                    q += L;
+                } else {
+                    if (li + (uint64_t)ws > nlit || q + 1 > elems) {
+                        rc = ORC_ERR_CORRUPT;
+                        break;
+                    }
+                    memcpy(chunk + (size_t)q * ws, lits + li, (size_t)ws);
+                    li += (uint64_t)ws;
+                    q += 1;
+                }
+            }
+            if (rc == 0 && (q != elems || seen != m)) rc = ORC_ERR_CORRUPT;
+        }
+        if (rc != 0) break;
+        uint64_t begin = c * (uint64_t)cs;
+        uint64_t take = n_bytes - begin;
+        if (take > (uint64_t)cs) take = (uint64_t)cs;
+        memcpy(out + begin, chunk, (size_t)take);
+    }
+    if (rc == 0 && (li != nlit || mi != nmat || flag_at != meta_bytes)) rc = ORC_ERR_CORRUPT;
+    free(chunk);
+    return rc;
+}

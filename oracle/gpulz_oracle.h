@@ -47,6 +47,17 @@ void orc_encode_chunk_range(const uint8_t* in, uint64_t n_bytes, int word_size, 
 int orc_decode_chunk_range(const uint8_t* in, uint64_t in_len, const uint64_t* block_off,
                            uint8_t* out, uint64_t n_bytes, uint64_t c0, uint64_t c1);
 
+/* Split mode: four ports (meta, literals, lengths, offsets) holding the same
+ * items. bounds[k] is an upper bound on port k's bytes; sizes[k] receives
+ * each port's length. */
+void orc_split_bounds(uint64_t n_bytes, int word_size, int chunk_size, uint64_t bounds[4]);
+int orc_compress_split(const uint8_t* in, uint64_t n_bytes, int word_size, int chunk_size,
+                       int match_level, uint8_t* meta, uint8_t* lits, uint8_t* lens,
+                       uint8_t* offs, uint64_t sizes[4]);
+int orc_decompress_split(const uint8_t* meta, const uint8_t* lits, const uint8_t* lens,
+                         const uint8_t* offs, const uint64_t port_len[4], uint8_t* out,
+                         uint64_t n_bytes);
+
 #ifdef __cplusplus
 }
 #endif
