@@ -156,6 +156,52 @@ gpulz_status gpulz_compress_noalloc(const void* d_in, size_t n_bytes, int word_s
                                     size_t capacity, size_t* d_out_bytes, cudaStream_t stream);
 
 /*
+ * Split mode (stage page, split-mode section; codebase note CN-GPULZ-1):
+ * the same items as gpulz_compress, emitted as four ports instead of one
+ * interleaved stream, so that a downstream entropy coder sees each kind of
+ * symbol on its own:
+ *   meta     -- 48-byte header {u32 magic "GPLZ", u16 version 2, u8 word_size,
+ *               u8 0, u32 chunk_size, u32 n_chunks, u64 orig_bytes,
+ *               u64 meta_bytes, u64 literal_bytes, u64 n_matches}, then
+ *               n_chunks entries {u32 n_items | RAW << 31, u32 n_matches}
+ *               ({0,0} zero chunk, {RAW,0} raw chunk), then every coded
+ *               chunk's flag words (ceil(n_items/32) u32, 1 = match, LSB
+ *               first), in chunk order;
+ *   literals -- every literal word (word_size bytes, as in the input) in
+ *               item order, chunk after chunk; a raw chunk's chunk_size
+ *               bytes (zero padded) land here whole;
+ *   lengths  -- one byte per match token, item order, chunk after chunk;
+ *   offsets  -- one byte per match token, likewise.
+ * Ports are back to back, without padding. The pages fix the ports' contents,
+ * not this byte layout, which is this library's.
+ */
+
+/* Upper bounds on the four ports' bytes, in the order meta, literals,
+ * lengths, offsets. */
+gpulz_status gpulz_split_bounds(size_t n_bytes, int word_size, int chunk_size, size_t bounds[4]);
+
+/* Split-mode encode. d_meta must be 4-byte aligned; the other ports have no
+ * alignment rule. capacity[4] (host) bounds each port in the same order;
+ * nothing is written at or past a port's capacity. The four port lengths are
+ * written on the device to d_port_bytes[0..3] (8-byte aligned); a port that
+ * did not fit is recorded as GPULZ_ERR_CAPACITY for gpulz_device_status().
+ * Other arguments and errors as gpulz_compress. */
+gpulz_status gpulz_compress_split(const void* d_in, size_t n_bytes, int word_size, int chunk_size,
+                                  int match_level, void* d_meta, void* d_literals,
+                                  void* d_lengths, void* d_offsets, const size_t capacity[4],
+                                  size_t* d_port_bytes, cudaStream_t stream);
+
+/* Split-mode decode straight out of the four ports (no rebuilt single
+ * stream): port_bytes[4] (host) gives each port's available bytes in the
+ * order meta, literals, lengths, offsets; d_meta must be 4-byte aligned; an
+ * empty port may be null. Output, n_bytes and errors as
+ * gpulz_decompress_bounded. */
+gpulz_status gpulz_decompress_split(const void* d_meta, const void* d_literals,
+                                    const void* d_lengths, const void* d_offsets,
+                                    const size_t port_bytes[4], void* d_out, size_t n_bytes,
+                                    cudaStream_t stream);
+
+/*
  * gpulz_set_kernel_events -- measurement hook (no counterpart in the paper).
  *
  * gpulz_compress runs three kernels (encode, tile scan of block sizes, copy to

@@ -20,7 +20,8 @@ __all__ = [
     "library_path", "load", "build", "gpulz_compress", "gpulz_compress_noalloc", "gpulz_decompress",
     "gpulz_decompress_bounded", "gpulz_compress_bound", "gpulz_stream_info",
     "gpulz_device_status", "gpulz_set_kernel_events", "gpulz_status_string", "compress",
-    "decompress",
+    "decompress", "gpulz_split_bounds", "gpulz_compress_split", "gpulz_decompress_split",
+    "compress_split", "decompress_split",
 ]
 
 GPULZ_OK = 0
@@ -76,6 +77,13 @@ def load():
     lib.gpulz_stream_info.restype = i32
     lib.gpulz_device_status.argtypes = [vp]
     lib.gpulz_device_status.restype = i32
+    szp = ctypes.POINTER(sz)
+    lib.gpulz_split_bounds.argtypes = [sz, i32, i32, szp]
+    lib.gpulz_split_bounds.restype = i32
+    lib.gpulz_compress_split.argtypes = [vp, sz, i32, i32, i32, vp, vp, vp, vp, szp, vp, vp]
+    lib.gpulz_compress_split.restype = i32
+    lib.gpulz_decompress_split.argtypes = [vp, vp, vp, vp, szp, vp, sz, vp]
+    lib.gpulz_decompress_split.restype = i32
     lib.gpulz_set_kernel_events.argtypes = [vp, vp]
     lib.gpulz_set_kernel_events.restype = i32
     lib.gpulz_status_string.argtypes = [i32]
@@ -151,6 +159,29 @@ def gpulz_device_status(stream=None) -> int:
     return load().gpulz_device_status(_stream(stream))
 
 
+def gpulz_split_bounds(n_bytes, word_size, chunk_size):
+    """Returns (status, [meta, literals, lengths, offsets] byte bounds)."""
+    b = (ctypes.c_size_t * 4)()
+    st = load().gpulz_split_bounds(n_bytes, word_size, chunk_size, b)
+    return st, [int(v) for v in b]
+
+
+def gpulz_compress_split(d_in, n_bytes, word_size, chunk_size, match_level, d_meta, d_literals,
+                         d_lengths, d_offsets, capacity, d_port_bytes, stream=None) -> int:
+    cap = (ctypes.c_size_t * 4)(*[int(v) for v in capacity])
+    return load().gpulz_compress_split(_ptr(d_in), n_bytes, word_size, chunk_size, match_level,
+                                       _ptr(d_meta), _ptr(d_literals), _ptr(d_lengths),
+                                       _ptr(d_offsets), cap, _ptr(d_port_bytes), _stream(stream))
+
+
+def gpulz_decompress_split(d_meta, d_literals, d_lengths, d_offsets, port_bytes, d_out, n_bytes,
+                           stream=None) -> int:
+    pb = (ctypes.c_size_t * 4)(*[int(v) for v in port_bytes])
+    return load().gpulz_decompress_split(_ptr(d_meta), _ptr(d_literals), _ptr(d_lengths),
+                                         _ptr(d_offsets), pb, _ptr(d_out), n_bytes,
+                                         _stream(stream))
+
+
 def gpulz_set_kernel_events(start, stop) -> int:
     """Measurement hook: bracket the encode/decode kernel of the following calls
     from this thread with two CUDA events (torch.cuda.Event, raw handles or
@@ -186,6 +217,37 @@ def compress(x, word_size: int, chunk_size: int, match_level: int, stream=None, 
     if st != GPULZ_OK:
         raise GpulzError(st, "gpulz_compress")
     return out, out_bytes
+
+
+def compress_split(x, word_size: int, chunk_size: int, match_level: int, stream=None):
+    """Split-mode encode of a contiguous CUDA tensor's bytes. Returns
+    ([meta, literals, lengths, offsets] tensors at their bounds, port_bytes)
+    where port_bytes (int64, 4 elements, on the device) holds the lengths."""
+    import torch
+    n = x.numel() * x.element_size()
+    st, bounds = gpulz_split_bounds(n, word_size, chunk_size)
+    if st != GPULZ_OK:
+        raise GpulzError(st, "gpulz_split_bounds")
+    ports = [torch.empty(max(b, 4), dtype=torch.uint8, device=x.device) for b in bounds]
+    port_bytes = torch.empty(4, dtype=torch.int64, device=x.device)
+    st = gpulz_compress_split(x if n else None, n, word_size, chunk_size, match_level, *ports,
+                              [p.numel() for p in ports], port_bytes, stream)
+    if st != GPULZ_OK:
+        raise GpulzError(st, "gpulz_compress_split")
+    return ports, port_bytes
+
+
+def decompress_split(ports, port_bytes, n_bytes: int, stream=None, out=None):
+    """Split-mode decode of four CUDA tensors (meta, literals, lengths,
+    offsets) with port_bytes[k] valid bytes each (host ints)."""
+    import torch
+    if out is None:
+        out = torch.empty(max(n_bytes, 1), dtype=torch.uint8, device=ports[0].device)
+    st = gpulz_decompress_split(*[p if p is not None and p.numel() else None for p in ports],
+                                port_bytes, out, n_bytes, stream)
+    if st != GPULZ_OK:
+        raise GpulzError(st, "gpulz_decompress_split")
+    return out[:n_bytes]
 
 
 def decompress(stream_buf, n_bytes: int, stream=None, out=None, in_bytes: int | None = None):

@@ -120,9 +120,12 @@ size_t gpulz_compress_bound(size_t n_bytes, int word_size, int chunk_size) {
     return (size_t)(kHeaderBytes + chunks * ((uint64_t)kEntryBytes + (uint64_t)chunk_size));
 }
 
-gpulz_status gpulz_compress(const void* d_in, size_t n_bytes, int word_size, int chunk_size,
-                            int match_level, void* d_out, size_t capacity, size_t* d_out_bytes,
-                            cudaStream_t stream) {
+namespace {
+// Shared by the single-stream and split encoders: argument checks, scratch,
+// and the launch. ports/port_cap are null for the single-stream form.
+gpulz_status compress_impl(const void* d_in, size_t n_bytes, int word_size, int chunk_size,
+                           int match_level, void* d_out, size_t capacity, size_t* d_out_bytes,
+                           uint8_t* const* ports, const size_t* port_cap, cudaStream_t stream) {
     if (!valid_geometry(word_size, chunk_size)) return GPULZ_ERR_INVALID_ARG;
     if (match_level != 0 && match_level != 1) return GPULZ_ERR_INVALID_ARG;
     if ((n_bytes > 0 && d_in == nullptr) || d_out == nullptr || d_out_bytes == nullptr)
@@ -146,8 +149,10 @@ gpulz_status gpulz_compress(const void* d_in, size_t n_bytes, int word_size, int
     a.desc = nullptr;
     a.slots = st + r.slots;
     a.sizes = reinterpret_cast<uint32_t*>(st + r.sizes);
+    a.msizes = a.sizes + s->cap_chunks;
     a.offsets = reinterpret_cast<uint64_t*>(st + r.offsets);
     a.tdesc = reinterpret_cast<uint64_t*>(st + r.tdesc);
+    a.tdesc_stride = tdesc_len(s->cap_chunks);
     a.ticket = tickets + 2 * epoch;
     a.ticket2 = tickets + 2 * epoch + 1;
     a.status = reinterpret_cast<uint32_t*>(s->base);
@@ -156,13 +161,51 @@ gpulz_status gpulz_compress(const void* d_in, size_t n_bytes, int word_size, int
     a.elems = (uint32_t)(chunk_size / word_size);
     a.n_chunks = (uint32_t)chunks;
     a.hash_bits = log2_exact(2u * a.elems);
+    a.split = ports != nullptr;
+    for (int k = 0; k < 3; ++k) {
+        a.port[k] = ports ? ports[k] : nullptr;
+        a.port_cap[k] = ports ? port_cap[k] : 0;
+    }
     if (launch_encode(a, word_size, match_level, false, stream) != cudaSuccess)
         return GPULZ_ERR_CUDA;
     return GPULZ_OK;
 }
+}  // namespace
 
-gpulz_status gpulz_decompress_bounded(const void* d_in, size_t in_bytes, void* d_out,
-                                      size_t n_bytes, cudaStream_t stream) {
+gpulz_status gpulz_compress(const void* d_in, size_t n_bytes, int word_size, int chunk_size,
+                            int match_level, void* d_out, size_t capacity, size_t* d_out_bytes,
+                            cudaStream_t stream) {
+    return compress_impl(d_in, n_bytes, word_size, chunk_size, match_level, d_out, capacity,
+                         d_out_bytes, nullptr, nullptr, stream);
+}
+
+gpulz_status gpulz_split_bounds(size_t n_bytes, int word_size, int chunk_size, size_t bounds[4]) {
+    if (!valid_geometry(word_size, chunk_size) || bounds == nullptr) return GPULZ_ERR_INVALID_ARG;
+    const uint64_t chunks = ((uint64_t)n_bytes + chunk_size - 1) / (uint64_t)chunk_size;
+    const uint64_t elems = (uint64_t)(chunk_size / word_size);
+    bounds[0] = (size_t)(kSplitHeaderBytes + kEntryBytes * chunks + 4u * chunks * ((elems + 31u) / 32u));
+    bounds[1] = (size_t)(chunks * (uint64_t)chunk_size);
+    bounds[2] = (size_t)(chunks * elems);
+    bounds[3] = (size_t)(chunks * elems);
+    return GPULZ_OK;
+}
+
+gpulz_status gpulz_compress_split(const void* d_in, size_t n_bytes, int word_size, int chunk_size,
+                                  int match_level, void* d_meta, void* d_literals,
+                                  void* d_lengths, void* d_offsets, const size_t capacity[4],
+                                  size_t* d_port_bytes, cudaStream_t stream) {
+    if (capacity == nullptr || d_literals == nullptr || d_lengths == nullptr || d_offsets == nullptr)
+        return GPULZ_ERR_INVALID_ARG;
+    uint8_t* const ports[3] = {static_cast<uint8_t*>(d_literals), static_cast<uint8_t*>(d_lengths),
+                               static_cast<uint8_t*>(d_offsets)};
+    return compress_impl(d_in, n_bytes, word_size, chunk_size, match_level, d_meta, capacity[0],
+                         d_port_bytes, ports, capacity + 1, stream);
+}
+
+namespace {
+gpulz_status decompress_impl(const void* d_in, size_t in_bytes, void* d_out, size_t n_bytes,
+                             const uint8_t* const* ports, const size_t* port_len,
+                             cudaStream_t stream) {
     if (d_in == nullptr || (n_bytes > 0 && d_out == nullptr)) return GPULZ_ERR_INVALID_ARG;
     if (!aligned(d_in, 4)) return GPULZ_ERR_INVALID_ARG;
     const uint64_t max_chunks = ((uint64_t)n_bytes + 1023u) / 1024u;
@@ -179,12 +222,38 @@ gpulz_status gpulz_decompress_bounded(const void* d_in, size_t in_bytes, void* d
     a.n_bytes = n_bytes;
     a.offsets = reinterpret_cast<uint64_t*>(st + r.offsets);
     a.tdesc = reinterpret_cast<uint64_t*>(st + r.tdesc);
+    a.tdesc_stride = tdesc_len(s->cap_chunks);
     a.ticket = tickets + 2 * epoch;
     a.ticket2 = tickets + 2 * epoch + 1;
     a.status = reinterpret_cast<uint32_t*>(s->base);
     a.epoch = epoch;
+    a.split = ports != nullptr;
+    for (int k = 0; k < 3; ++k) {
+        a.port[k] = ports ? ports[k] : nullptr;
+        a.port_len[k] = ports ? port_len[k] : 0;
+    }
     if (launch_decode(a, stream) != cudaSuccess) return GPULZ_ERR_CUDA;
     return GPULZ_OK;
+}
+}  // namespace
+
+gpulz_status gpulz_decompress_bounded(const void* d_in, size_t in_bytes, void* d_out,
+                                      size_t n_bytes, cudaStream_t stream) {
+    return decompress_impl(d_in, in_bytes, d_out, n_bytes, nullptr, nullptr, stream);
+}
+
+gpulz_status gpulz_decompress_split(const void* d_meta, const void* d_literals,
+                                    const void* d_lengths, const void* d_offsets,
+                                    const size_t port_bytes[4], void* d_out, size_t n_bytes,
+                                    cudaStream_t stream) {
+    if (port_bytes == nullptr) return GPULZ_ERR_INVALID_ARG;
+    // a null port counts as empty: every read of a port is bounded by its length
+    const uint8_t* const ports[3] = {static_cast<const uint8_t*>(d_literals),
+                                     static_cast<const uint8_t*>(d_lengths),
+                                     static_cast<const uint8_t*>(d_offsets)};
+    const size_t lens[3] = {d_literals ? port_bytes[1] : 0, d_lengths ? port_bytes[2] : 0,
+                            d_offsets ? port_bytes[3] : 0};
+    return decompress_impl(d_meta, port_bytes[0], d_out, n_bytes, ports, lens, stream);
 }
 
 gpulz_status gpulz_decompress(const void* d_in, void* d_out, size_t n_bytes, cudaStream_t stream) {

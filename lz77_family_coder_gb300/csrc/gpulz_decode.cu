@@ -33,6 +33,7 @@ constexpr uint16_t kLit = 0x8000u;
 struct Geo {
     uint32_t ws, cs, E, C;
     uint64_t orig, total, body0;
+    uint64_t lit_total, m_total;  // split mode: literal bytes and matches in the ports
 };
 
 __device__ __forceinline__ uint32_t align16d(uint32_t v) { return (v + 15u) & ~15u; }
@@ -54,6 +55,37 @@ __device__ __forceinline__ DecSlot dec_slot(uint32_t cs, uint32_t E) {
 
 __device__ __forceinline__ uint32_t read_u32(const uint8_t* p) {
     return *reinterpret_cast<const uint32_t*>(p);
+}
+// Four bytes at any address (split-mode ports have no alignment rule).
+__device__ __forceinline__ uint32_t read_u32_any(const uint8_t* p) {
+    if ((reinterpret_cast<uintptr_t>(p) & 3u) == 0) return read_u32(p);
+    return (uint32_t)p[0] | ((uint32_t)p[1] << 8) | ((uint32_t)p[2] << 16) | ((uint32_t)p[3] << 24);
+}
+// Copy n bytes from any address into a warp's shared-memory data area.
+__device__ __forceinline__ void stage_bytes(uint8_t* dst, const uint8_t* src, uint32_t n, int lane) {
+    if (((reinterpret_cast<uintptr_t>(src) | reinterpret_cast<uintptr_t>(dst) | n) & 3u) == 0) {
+        for (uint32_t i = 4u * lane; i < n; i += 128u)
+            *reinterpret_cast<uint32_t*>(dst + i) = read_u32(src + i);
+    } else {
+        for (uint32_t i = lane; i < n; i += 32u) dst[i] = src[i];
+    }
+}
+
+// Split mode: a chunk's (flag words, literal bytes, matches) from its entry;
+// false if the entry is invalid.
+__device__ __forceinline__ bool split_entry(uint32_t items, uint32_t m, const Geo& g, uint32_t& fw,
+                                            uint32_t& lit) {
+    fw = 0;
+    lit = 0;
+    if (items == 0 && m == 0) return true;
+    if (items == kRawBit && m == 0) {
+        lit = g.cs;
+        return true;
+    }
+    if ((items & kRawBit) || items > g.E || m > items) return false;
+    fw = (items + 31u) / 32u;
+    lit = g.ws * (items - m);
+    return lit + 2u * m <= g.cs;
 }
 
 // Block size of a size-table entry; 0xFFFFFFFF if the entry is invalid.
@@ -126,12 +158,29 @@ __device__ void decode_chunks(const DecodeArgs& a, const Geo& g, uint8_t* slot_b
         }
         if (c >= g.C) break;
 
-        const uint8_t* e = a.in + kHeaderBytes + (uint64_t)kEntryBytes * c;
-        const uint32_t items = read_u32(e), dbytes = read_u32(e + 4);
-        uint32_t blk = entry_block(items, dbytes, g);
-        bool bad = blk == 0xFFFFFFFFu;
-        const uint64_t src_off = a.offsets[c];
-        if (!bad && (src_off < g.body0 || src_off + blk > g.total)) bad = true;
+        const bool split = a.split != 0;
+        const uint8_t* e = a.in + (split ? kSplitHeaderBytes : kHeaderBytes) + (uint64_t)kEntryBytes * c;
+        const uint32_t items = read_u32(e), second = read_u32(e + 4);
+        // single stream: second = data bytes; split: second = matches
+        uint32_t dbytes = second, blk = 0, sfw = 0, slit = 0;
+        bool bad;
+        uint64_t src_off = 0, s_of = 0, s_ol = 0, s_om = 0;
+        if (!split) {
+            blk = entry_block(items, dbytes, g);
+            bad = blk == 0xFFFFFFFFu;
+            src_off = a.offsets[c];
+            if (!bad && (src_off < g.body0 || src_off + blk > g.total)) bad = true;
+        } else {
+            bad = !split_entry(items, second, g, sfw, slit);
+            s_of = a.offsets[3ull * c];
+            s_ol = a.offsets[3ull * c + 1];
+            s_om = a.offsets[3ull * c + 2];
+            if (!bad && (g.body0 + 4ull * (s_of + sfw) > g.total || s_ol + slit > g.lit_total ||
+                         s_om + second > g.m_total))
+                bad = true;
+            blk = (items == 0 && second == 0) ? 0u : 1u;
+            dbytes = slit + 2u * second;
+        }
 
         const uint64_t begin = (uint64_t)c * CS;
         const uint64_t avail = g.orig - begin;
@@ -149,16 +198,37 @@ __device__ void decode_chunks(const DecodeArgs& a, const Geo& g, uint8_t* slot_b
         }
         const uint8_t* src = a.in + src_off;
         if (items == kRawBit) {
-            write_chunk(out, take, chunk_out_aligned, lane,
-                        [src](uint32_t j) { return read_u32(src + 4u * j); });
+            if (split) {
+                const uint8_t* lsrc = a.port[0] + s_ol;
+                write_chunk(out, take, chunk_out_aligned, lane,
+                            [lsrc](uint32_t j) { return read_u32_any(lsrc + 4u * j); });
+            } else {
+                write_chunk(out, take, chunk_out_aligned, lane,
+                            [src](uint32_t j) { return read_u32(src + 4u * j); });
+            }
             continue;
         }
 
         // ---- D2: load flags and items into shared memory ----
         const uint32_t fw = (items + 31u) / 32u;
-        const uint32_t dw = (dbytes + 3u) / 4u;
-        // four loads in flight per lane
-        for (uint32_t j0 = lane; j0 < fw + dw; j0 += 128) {
+        const uint32_t dw = split ? 0u : (dbytes + 3u) / 4u;
+        if (split) {
+            // flags from the meta port; literals, lengths and offsets from
+            // theirs, into [literals | lengths | offsets] of the data area
+            const uint8_t* fsrc = a.in + g.body0 + 4ull * s_of;
+            for (uint32_t j = lane; j < fw; j += 32) {
+                uint32_t v = read_u32(fsrc + 4u * j);
+                if (j == fw - 1u && (items & 31u)) v &= (1u << (items & 31u)) - 1u;
+                s_fl[j] = v;
+            }
+            stage_bytes(s_data, a.port[0] + s_ol, slit, lane);
+            stage_bytes(s_data + slit, a.port[1] + s_om, second, lane);
+            stage_bytes(s_data + slit + second, a.port[2] + s_om, second, lane);
+        }
+        // single stream: flags and items from the block, four loads in flight
+        // per lane (split mode staged them above)
+        const uint32_t nwords = split ? 0u : fw + dw;
+        for (uint32_t j0 = lane; j0 < nwords; j0 += 128) {
             uint32_t vv[4];
 #pragma unroll
             for (int u = 0; u < 4; ++u) {
@@ -194,7 +264,7 @@ __device__ void decode_chunks(const DecodeArgs& a, const Geo& g, uint8_t* slot_b
             run += __shfl_sync(FULL, incl, 31);
         }
         const uint32_t n_match = run;
-        if ((uint64_t)WS * (items - n_match) + 2ull * n_match != dbytes) {
+        if (split ? n_match != second : (uint64_t)WS * (items - n_match) + 2ull * n_match != dbytes) {
             if (lane == 0) atomicOr(a.status, kStatCorrupt);
             continue;
         }
@@ -210,7 +280,7 @@ __device__ void decode_chunks(const DecodeArgs& a, const Geo& g, uint8_t* slot_b
             bool ism = (w >> (j & 31u)) & 1u;
             if (ism) {
                 uint32_t pm = s_wp[j >> 5] + __popc(w & ((1u << (j & 31u)) - 1u));
-                uint32_t b = WS * j - (WS - 2u) * pm;
+                uint32_t b = split ? slit + pm : WS * j - (WS - 2u) * pm;
                 span_sum += s_data[b];
             } else {
                 span_sum += 1u;
@@ -235,9 +305,12 @@ __device__ void decode_chunks(const DecodeArgs& a, const Geo& g, uint8_t* slot_b
             uint32_t w = s_fl[j >> 5];
             bool ism = (w >> (j & 31u)) & 1u;
             uint32_t pm = s_wp[j >> 5] + __popc(w & ((1u << (j & 31u)) - 1u));
-            uint32_t b = WS * j - (WS - 2u) * pm;
+            // single stream: the item's token or literal at b; split: the
+            // literal at WS * (literals before it), length and offset bytes
+            // at slit + pm and slit + matches + pm
+            uint32_t b = split ? (ism ? slit + pm : WS * (j - pm)) : WS * j - (WS - 2u) * pm;
             if (ism) {
-                uint32_t L = s_data[b], O = s_data[b + 1];
+                uint32_t L = s_data[b], O = s_data[split ? slit + second + pm : b + 1];
                 if (L == 0 || O == 0 || O > q) {
                     lane_bad = true;
                     break;
@@ -296,23 +369,29 @@ __device__ void decode_chunks(const DecodeArgs& a, const Geo& g, uint8_t* slot_b
 __device__ bool parse_header(const DecodeArgs& a, Geo& g) {
     const int lane = threadIdx.x & 31;
     uint32_t hw = 0;
-    const bool hdr_fits = a.in_bytes >= kHeaderBytes;
-    if (lane < 8 && hdr_fits) hw = read_u32(a.in + 4 * lane);
-    uint32_t h[8];
+    const uint32_t hdr = a.split ? kSplitHeaderBytes : kHeaderBytes;
+    const bool hdr_fits = a.in_bytes >= hdr;
+    if (lane < (int)(hdr / 4u) && hdr_fits) hw = read_u32(a.in + 4 * lane);
+    uint32_t h[12];
 #pragma unroll
-    for (int k = 0; k < 8; ++k) h[k] = __shfl_sync(FULL, hw, k);
+    for (int k = 0; k < 12; ++k) h[k] = __shfl_sync(FULL, hw, k);
     g.ws = (h[1] >> 16) & 0xFFu;
     g.cs = h[2];
     g.C = h[3];
     g.orig = (uint64_t)h[4] | ((uint64_t)h[5] << 32);
     g.total = (uint64_t)h[6] | ((uint64_t)h[7] << 32);
-    bool ok = hdr_fits && h[0] == kMagic && (h[1] & 0xFFFFu) == kVersion && (h[1] >> 24) == 0 &&
-              valid_geometry((int)g.ws, (int)g.cs);
+    g.lit_total = a.split ? ((uint64_t)h[8] | ((uint64_t)h[9] << 32)) : 0;
+    g.m_total = a.split ? ((uint64_t)h[10] | ((uint64_t)h[11] << 32)) : 0;
+    bool ok = hdr_fits && h[0] == kMagic && (h[1] & 0xFFFFu) == (a.split ? kSplitVersion : kVersion) &&
+              (h[1] >> 24) == 0 && valid_geometry((int)g.ws, (int)g.cs);
     if (ok) {
         g.E = g.cs / g.ws;
         ok = (uint64_t)g.C == (g.orig + g.cs - 1) / g.cs;
-        g.body0 = (uint64_t)kHeaderBytes + (uint64_t)kEntryBytes * g.C;
+        g.body0 = (uint64_t)hdr + (uint64_t)kEntryBytes * g.C;
         ok = ok && g.total >= g.body0 && g.total <= a.in_bytes;
+        if (a.split)
+            ok = ok && g.lit_total <= a.port_len[0] && g.m_total <= a.port_len[1] &&
+                 g.m_total <= a.port_len[2];
     }
     if (!ok) {
         if (blockIdx.x == 0 && threadIdx.x == 0) atomicOr(a.status, kStatCorrupt);
@@ -338,12 +417,37 @@ __global__ void __launch_bounds__(kScanThreads) offsets_kernel(DecodeArgs a) {
         __syncthreads();
         const uint32_t t = sm.tile;
         if (t >= n_tiles) break;
+        const uint32_t c0 = t * kTile;
+        if (a.split) {
+            // three scans: flag words, literal bytes, matches (an invalid entry
+            // counts 0 and fails in the decode kernel)
+            uint64_t tot[3];
+#pragma unroll
+            for (int k = 0; k < 3; ++k) {
+                const uint64_t prefix = tile_scan(
+                    sm, t, g.C, a.tdesc + (uint64_t)k * a.tdesc_stride, a.epoch, a.status, [&](uint32_t c) {
+                        const uint8_t* e = a.in + kSplitHeaderBytes + (uint64_t)kEntryBytes * c;
+                        const uint32_t items = read_u32(e), m = read_u32(e + 4);
+                        uint32_t fw, lit;
+                        if (!split_entry(items, m, g, fw, lit)) return 0u;
+                        return k == 0 ? fw : (k == 1 ? lit : m);
+                    });
+                for (uint32_t j = (uint32_t)tid; j < kTile && c0 + j < g.C; j += kScanThreads)
+                    a.offsets[3ull * (c0 + j) + k] = prefix + sm.off[j];
+                tot[k] = prefix + sm.total;
+                __syncthreads();
+            }
+            if (t == n_tiles - 1 && tid == 0 &&
+                (g.body0 + 4ull * tot[0] != g.total || tot[1] != g.lit_total || tot[2] != g.m_total))
+                atomicOr(a.status, kStatCorrupt);
+            __syncthreads();
+            continue;
+        }
         const uint64_t prefix = tile_scan(sm, t, g.C, a.tdesc, a.epoch, a.status, [&](uint32_t c) {
             const uint8_t* e = a.in + kHeaderBytes + (uint64_t)kEntryBytes * c;
             const uint32_t b = entry_block(read_u32(e), read_u32(e + 4), g);
             return b == 0xFFFFFFFFu ? 0u : b;
         });
-        const uint32_t c0 = t * kTile;
         for (uint32_t j = (uint32_t)tid; j < kTile && c0 + j < g.C; j += kScanThreads)
             a.offsets[c0 + j] = g.body0 + prefix + sm.off[j];
         if (t == n_tiles - 1 && tid == 0 && g.body0 + prefix + sm.total != g.total)

@@ -139,6 +139,25 @@ __device__ void write_header(const EncodeArgs& a, uint32_t ws, uint64_t total) {
     if (total > a.capacity) atomicOr(a.status, kStatCapacity);
 }
 
+// Split mode: the meta port's 48-byte header and the four port lengths.
+__device__ void write_header_split(const EncodeArgs& a, uint32_t ws, uint64_t meta_bytes,
+                                   uint64_t lit_bytes, uint64_t matches) {
+    const uint32_t h[12] = {kMagic, kSplitVersion | (ws << 16), a.chunk_size, a.n_chunks,
+                            (uint32_t)a.n_bytes, (uint32_t)(a.n_bytes >> 32),
+                            (uint32_t)meta_bytes, (uint32_t)(meta_bytes >> 32),
+                            (uint32_t)lit_bytes, (uint32_t)(lit_bytes >> 32),
+                            (uint32_t)matches, (uint32_t)(matches >> 32)};
+#pragma unroll
+    for (int k = 0; k < 12; ++k) store_u32_capped(a.out, 4ull * k, h[k], a.capacity);
+    a.out_bytes[0] = meta_bytes;
+    a.out_bytes[1] = lit_bytes;
+    a.out_bytes[2] = matches;
+    a.out_bytes[3] = matches;
+    if (meta_bytes > a.capacity || lit_bytes > a.port_cap[0] || matches > a.port_cap[1] ||
+        matches > a.port_cap[2])
+        atomicOr(a.status, kStatCapacity);
+}
+
 // ---------------------------------------------------------------------------
 // Per-segment near masks (E3): m[p] bit o-1 set iff element (base+p) equals
 // element (base+p-o), 1 <= o <= 32, base+p-o >= 0.
@@ -235,7 +254,7 @@ __global__ void __launch_bounds__(256, 4) encode_kernel(EncodeArgs a) {
         const uint32_t c = (SINGLE || !have) ? t : (t == 0 ? a.n_chunks - 1u : t - 1u);
 
         bool nonzero = false;
-        uint32_t items = 0, dbytes = 0, blk = 0, entry_items = 0;
+        uint32_t items = 0, dbytes = 0, blk = 0, entry_items = 0, n_match = 0;
         uint32_t path = 0, mmask = 0, item_base = 0, match_base = 0;
         if (have) {
             // ---- E1: load the chunk (zero padded) ----
@@ -537,8 +556,8 @@ __global__ void __launch_bounds__(256, 4) encode_kernel(EncodeArgs a) {
                     item_base = excl & 0xFFFFu;
                     match_base = excl >> 16;
                     items = total & 0xFFFFu;
-                    const uint32_t matches = total >> 16;
-                    dbytes = WS * (items - matches) + 2u * matches;
+                    n_match = total >> 16;
+                    dbytes = WS * (items - n_match) + 2u * n_match;
                 }
                 // ---- E8: raw fallback ----
                 blk = 4u * ((items + 31u) / 32u) + ((dbytes + 3u) & ~3u);
@@ -597,7 +616,36 @@ __global__ void __launch_bounds__(256, 4) encode_kernel(EncodeArgs a) {
                 for (uint32_t k = tid; k < fw; k += nthreads) s_fl[k] = 0;
                 __syncthreads();
                 uint32_t bb = WS * (item_base - match_base) + 2u * match_base;
-                uint32_t fbits = 0, k = 0, rem = path;
+                if (a.split) {
+                    // split mode: the chunk's literals, then its lengths, then its
+                    // offsets, each in item order (the same bytes, regrouped)
+                    const uint32_t lit_bytes = WS * (items - n_match);
+                    uint32_t li = WS * (item_base - match_base), mi = match_base;
+                    uint32_t fbits = 0, k = 0, rem = path;
+                    while (rem) {
+                        const uint32_t p = (uint32_t)__ffs(rem) - 1u;
+                        rem &= rem - 1u;
+                        const uint32_t pos = seg_a + p;
+                        if ((mmask >> p) & 1u) {
+                            const uint32_t lo = s_lo[pos];
+                            s_data[lit_bytes + mi] = (uint8_t)lo;
+                            s_data[lit_bytes + n_match + mi] = (uint8_t)(lo >> 8);
+                            ++mi;
+                            fbits |= 1u << k;
+                        } else {
+                            const uint32_t v = el_get<WS>(s_el, pos);
+                            if (WS == 1) s_data[li] = (uint8_t)v;
+                            else if (WS == 2) *reinterpret_cast<uint16_t*>(s_data + li) = (uint16_t)v;
+                            else *reinterpret_cast<uint32_t*>(s_data + li) = v;
+                            li += WS;
+                        }
+                        ++k;
+                    }
+                    if (fbits) or_bits(s_fl, item_base, fbits);
+                    if (tid == 0)
+                        for (uint32_t z = dbytes; z < ((dbytes + 3u) & ~3u); ++z) s_data[z] = 0;
+                }
+                uint32_t fbits = 0, k = 0, rem = a.split ? 0u : path;
                 while (rem) {
                     const uint32_t p = (uint32_t)__ffs(rem) - 1u;
                     rem &= rem - 1u;
@@ -626,9 +674,11 @@ __global__ void __launch_bounds__(256, 4) encode_kernel(EncodeArgs a) {
                     }
                     ++k;
                 }
-                if (fbits) or_bits(s_fl, item_base, fbits);
-                if (tid == 0)
-                    for (uint32_t z = dbytes; z < ((dbytes + 3u) & ~3u); ++z) s_data[z] = 0;
+                if (!a.split) {
+                    if (fbits) or_bits(s_fl, item_base, fbits);
+                    if (tid == 0)
+                        for (uint32_t z = dbytes; z < ((dbytes + 3u) & ~3u); ++z) s_data[z] = 0;
+                }
             }
         }
         p_c = c;
@@ -647,10 +697,21 @@ __global__ void __launch_bounds__(256, 4) encode_kernel(EncodeArgs a) {
                 *reinterpret_cast<uint32_t*>(slot + 4u * j) = v;
             }
             if (tid == 0) {
-                a.sizes[c] = blk;
-                const uint64_t eo = (uint64_t)kHeaderBytes + (uint64_t)kEntryBytes * c;
-                store_u32_capped(a.out, eo, p_entry, a.capacity);
-                store_u32_capped(a.out, eo + 4, p_dbytes, a.capacity);
+                if (a.split) {
+                    // literal bytes (the whole chunk if raw), matches, flag words
+                    const bool raw = p_entry == kRawBit;
+                    const uint32_t m = (nonzero && !raw) ? n_match : 0u;
+                    a.sizes[c] = !nonzero ? 0u : (raw ? CS : WS * (items - n_match));
+                    a.msizes[c] = m | (fw << 16);
+                    const uint64_t eo = (uint64_t)kSplitHeaderBytes + (uint64_t)kEntryBytes * c;
+                    store_u32_capped(a.out, eo, p_entry, a.capacity);
+                    store_u32_capped(a.out, eo + 4, m, a.capacity);
+                } else {
+                    a.sizes[c] = blk;
+                    const uint64_t eo = (uint64_t)kHeaderBytes + (uint64_t)kEntryBytes * c;
+                    store_u32_capped(a.out, eo, p_entry, a.capacity);
+                    store_u32_capped(a.out, eo + 4, p_dbytes, a.capacity);
+                }
             }
             __syncthreads();  // staging is free again
         }
@@ -712,6 +773,82 @@ __global__ void __launch_bounds__(kCopyWarps * 32) copy_pass(EncodeArgs a) {
     }
 }
 
+// ---------------------------------------------------------------------------
+// Pack pass, split mode. offsets_pass_split: per tile of kTile chunks, three
+// scans (flag words, literal bytes, matches), each with its own tile
+// descriptors and look-back; the last tile writes the meta header and the
+// port lengths. copy_pass_split: one warp per chunk moves its flag words to
+// the meta port (after the header and size table) and its literals, lengths
+// and offsets to their ports, nothing at or past a port's capacity.
+// ---------------------------------------------------------------------------
+__global__ void __launch_bounds__(kScanThreads) offsets_pass_split(EncodeArgs a, uint32_t ws) {
+    __shared__ TileSmem sm;
+    const int tid = threadIdx.x;
+    pdl_trigger();
+    pdl_wait();  // the encode kernel's sizes
+    const uint32_t n_tiles = (a.n_chunks + kTile - 1) / kTile;
+    if (a.n_chunks == 0) {
+        if (blockIdx.x == 0 && tid == 0)
+            write_header_split(a, ws, kSplitHeaderBytes, 0, 0);
+        return;
+    }
+    for (;;) {
+        if (tid == 0) sm.tile = atomicAdd(a.ticket2, 1u);
+        __syncthreads();
+        const uint32_t t = sm.tile;
+        if (t >= n_tiles) break;
+        const uint32_t c0 = t * kTile;
+        uint64_t tot[3];
+#pragma unroll
+        for (int k = 0; k < 3; ++k) {
+            const uint64_t prefix =
+                tile_scan(sm, t, a.n_chunks, a.tdesc + (uint64_t)k * a.tdesc_stride, a.epoch, a.status,
+                          [&](uint32_t c) {
+                              return k == 0 ? a.msizes[c] >> 16 : (k == 1 ? a.sizes[c] : a.msizes[c] & 0xFFFFu);
+                          });
+            for (uint32_t j = (uint32_t)tid; j < kTile && c0 + j < a.n_chunks; j += kScanThreads)
+                a.offsets[3ull * (c0 + j) + k] = prefix + sm.off[j];
+            tot[k] = prefix + sm.total;
+            __syncthreads();
+        }
+        if (t == n_tiles - 1 && tid == 0)
+            write_header_split(a, ws,
+                               (uint64_t)kSplitHeaderBytes + (uint64_t)kEntryBytes * a.n_chunks + 4ull * tot[0],
+                               tot[1], tot[2]);
+        __syncthreads();
+    }
+}
+
+__device__ __forceinline__ void copy_bytes_capped(uint8_t* dst, uint64_t at, uint64_t cap,
+                                                  const uint8_t* src, uint32_t n, int lane) {
+    if (((at | n | reinterpret_cast<uintptr_t>(src) | reinterpret_cast<uintptr_t>(dst)) & 3u) == 0) {
+        for (uint32_t i = 4u * lane; i < n; i += 128u)
+            if (at + i + 4 <= cap)
+                *reinterpret_cast<uint32_t*>(dst + at + i) = *reinterpret_cast<const uint32_t*>(src + i);
+    } else {
+        for (uint32_t i = lane; i < n; i += 32u)
+            if (at + i < cap) dst[at + i] = src[i];
+    }
+}
+
+__global__ void __launch_bounds__(kCopyWarps * 32) copy_pass_split(EncodeArgs a) {
+    const int lane = threadIdx.x & 31;
+    pdl_wait();  // the offsets (and, through them, the slots)
+    const uint32_t gw = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+    const uint32_t nw = (gridDim.x * blockDim.x) >> 5;
+    const uint64_t flags0 = (uint64_t)kSplitHeaderBytes + (uint64_t)kEntryBytes * a.n_chunks;
+    for (uint32_t c = gw; c < a.n_chunks; c += nw) {
+        const uint32_t ms = a.msizes[c];
+        const uint32_t fw = ms >> 16, m = ms & 0xFFFFu, lit = a.sizes[c];
+        const uint64_t* o = a.offsets + 3ull * c;
+        const uint8_t* src = a.slots + (uint64_t)c * a.chunk_size;
+        copy_bytes_capped(a.out, flags0 + 4ull * o[0], a.capacity, src, 4u * fw, lane);
+        copy_bytes_capped(a.port[0], o[1], a.port_cap[0], src + 4u * fw, lit, lane);
+        copy_bytes_capped(a.port[1], o[2], a.port_cap[1], src + 4u * fw + lit, m, lane);
+        copy_bytes_capped(a.port[2], o[2], a.port_cap[2], src + 4u * fw + lit + m, m, lane);
+    }
+}
+
 struct LaunchShape {
     int dev = -1;
     uint32_t smem = 0;
@@ -766,8 +903,8 @@ cudaError_t launch_t(const EncodeArgs& a, cudaStream_t stream) {
         uint64_t sgrid = (uint64_t)shape.sms * 4u;
         if (sgrid > tiles) sgrid = tiles;
         if (sgrid < 1) sgrid = 1;
-        if ((err = pdl_launch(offsets_pass, dim3((unsigned)sgrid), dim3(kScanThreads), 0, stream, a,
-                              (uint32_t)WS)) != cudaSuccess)
+        if ((err = pdl_launch(a.split ? offsets_pass_split : offsets_pass, dim3((unsigned)sgrid),
+                              dim3(kScanThreads), 0, stream, a, (uint32_t)WS)) != cudaSuccess)
             return err;
         if (a.n_chunks > 0) {
             if ((err = shape_for(copy_pass, kCopyWarps * 32, 0, shape_copy)) != cudaSuccess)
@@ -775,7 +912,8 @@ cudaError_t launch_t(const EncodeArgs& a, cudaStream_t stream) {
             uint64_t cgrid = (uint64_t)shape_copy.sms * (uint64_t)shape_copy.per_sm;
             const uint64_t need = (a.n_chunks + kCopyWarps - 1) / kCopyWarps;
             if (cgrid > need) cgrid = need;
-            err = pdl_launch(copy_pass, dim3((unsigned)cgrid), dim3(kCopyWarps * 32), 0, stream, a);
+            err = pdl_launch(a.split ? copy_pass_split : copy_pass, dim3((unsigned)cgrid),
+                             dim3(kCopyWarps * 32), 0, stream, a);
         }
     }
     return err;

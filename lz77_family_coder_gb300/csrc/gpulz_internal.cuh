@@ -12,6 +12,13 @@ constexpr uint32_t kVersion = 1u;
 constexpr uint32_t kHeaderBytes = 32u;
 constexpr uint32_t kEntryBytes = 8u;
 constexpr uint32_t kRawBit = 0x80000000u;
+// split mode (four ports): meta = 48-byte header {u32 magic, u16 version 2,
+// u8 word_size, u8 0, u32 chunk_size, u32 n_chunks, u64 orig_bytes,
+// u64 meta_bytes, u64 literal_bytes, u64 n_matches}, the size table
+// {u32 n_items | RAW << 31, u32 n_matches} per chunk, then every coded
+// chunk's flag words; literals, lengths and offsets back to back
+constexpr uint32_t kSplitVersion = 2u;
+constexpr uint32_t kSplitHeaderBytes = 48u;
 
 // ---- method constants (GPULZ stage page, match-search section) ----
 constexpr int kWindow = 32;     // near window, elements
@@ -50,14 +57,17 @@ struct ScratchRegions {
     size_t tdesc, offsets, sizes, slots, end;  // byte offsets from the state base
 };
 // cap_chunks: chunks the per-chunk arrays can hold; slot_bytes: bytes of block
-// slots (chunks x chunk_size for the two-pass encode, 0 otherwise).
+// slots (chunks x chunk_size for the two-pass encode, 0 otherwise). Three
+// tile-descriptor arrays, three u64 offsets and two u32 sizes per chunk (the
+// single-stream form uses the first of each; split mode all three).
+__host__ __device__ constexpr uint64_t tdesc_len(uint64_t cap_chunks) { return cap_chunks / kTile + 2; }
 __host__ __device__ constexpr ScratchRegions scratch_regions(uint64_t cap_chunks,
                                                             uint64_t slot_bytes) {
     ScratchRegions r{};
     r.tdesc = 0;
-    r.offsets = 8 * (cap_chunks / kTile + 2);         // u64 per chunk
-    r.sizes = r.offsets + 8 * cap_chunks;             // u32 per chunk
-    r.slots = (r.sizes + 4 * cap_chunks + 255) & ~(size_t)255;
+    r.offsets = 3 * 8 * tdesc_len(cap_chunks);        // 3 x u64 per chunk
+    r.sizes = r.offsets + 3 * 8 * cap_chunks;         // 2 x u32 per chunk
+    r.slots = (r.sizes + 2 * 4 * cap_chunks + 255) & ~(size_t)255;
     r.end = r.slots + slot_bytes;
     return r;
 }
@@ -293,10 +303,18 @@ struct EncodeArgs {
     unsigned long long* out_bytes;
     uint64_t* desc;     // single pass: per chunk aggregate, then inclusive prefix
     uint8_t* slots;     // two pass: chunk c's block at slots + c * chunk_size
-    uint32_t* sizes;    // two pass: chunk c's block size
-    uint64_t* offsets;  // two pass: chunk c's block offset in the stream
-    uint64_t* tdesc;    // two pass: tile descriptors of the pack pass
+    uint32_t* sizes;    // two pass: chunk c's block size (split: its literal bytes)
+    uint32_t* msizes;   // split: chunk c's matches | flag words << 16
+    uint64_t* offsets;  // two pass: chunk c's block offset (split: 3 per chunk,
+                        // flag bytes / literal bytes / matches before it)
+    uint64_t* tdesc;    // two pass: tile descriptors of the pack pass (split: 3 arrays)
+    uint64_t tdesc_stride;  // split: distance between the descriptor arrays
     uint32_t* ticket2;  // two pass: tile ticket of the pack pass
+    // split mode: out/capacity is the meta port; three more ports, and
+    // out_bytes points at 4 u64 (meta, literals, lengths, offsets)
+    uint32_t split;
+    uint8_t* port[3];
+    uint64_t port_cap[3];
     uint32_t* ticket;
     uint32_t* status;
     uint32_t epoch;
@@ -317,6 +335,13 @@ struct DecodeArgs {
     uint32_t* ticket2;  // chunk ticket of the decode pass
     uint32_t* status;
     uint32_t epoch;
+    // split mode: `in` is the meta port; three more ports with their lengths;
+    // offsets then holds 3 per chunk (flag words, literal bytes, matches before
+    // it) and tdesc 3 arrays tdesc_stride apart
+    uint32_t split;
+    const uint8_t* port[3];
+    uint64_t port_len[3];
+    uint64_t tdesc_stride;
 };
 
 // Programmatic dependent launch: a kernel launched with pdl_launch() may be

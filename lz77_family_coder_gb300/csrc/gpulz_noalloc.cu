@@ -102,7 +102,14 @@ extern "C" gpulz_status gpulz_compress_noalloc(const void* d_in, size_t n_bytes,
     a.desc = reinterpret_cast<uint64_t*>(base + kNoAllocHead);
     a.slots = nullptr;
     a.sizes = nullptr;
+    a.msizes = nullptr;
     a.offsets = nullptr;
+    a.tdesc_stride = 0;
+    a.split = 0;
+    for (int k = 0; k < 3; ++k) {
+        a.port[k] = nullptr;
+        a.port_cap[k] = 0;
+    }
     a.tdesc = nullptr;
     a.ticket2 = nullptr;
     a.ticket = reinterpret_cast<uint32_t*>(base + 4);
