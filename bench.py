@@ -47,6 +47,8 @@ def parse_args():
     p.add_argument("--config", type=int, default=CFG_ID)
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-e2e", action="store_true")
+    p.add_argument("--split", action="store_true",
+                   help="time split mode (four ports) instead of the single stream; one GPU")
     return p.parse_args()
 
 
@@ -468,10 +470,85 @@ def run_reference(args):
     print(json.dumps(line), flush=True)
 
 
+def run_split(args):
+    """Split mode (four ports) on one GPU: encode + decode per step, device
+    timed with CUDA events, L2 flushed between steps, ports checked against
+    the oracle's after timing."""
+    import numpy as np
+    import torch
+    import synth
+    import lz77_family_coder_gb300 as g
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(0)
+    g.load()
+    cfg = synth.CONFIGS[args.config]
+    ws, cs, lvl = cfg.word_size, cfg.chunk_size, cfg.match_level
+    x = synth.generate(cfg)
+    n = x.size
+    d_in = torch.from_numpy(x).to(dev)
+    st, bounds = g.gpulz_split_bounds(n, ws, cs)
+    assert st == g.GPULZ_OK
+    ports = [torch.empty(max(b, 4), dtype=torch.uint8, device=dev) for b in bounds]
+    caps = [p.numel() for p in ports]
+    pb = torch.zeros(4, dtype=torch.int64, device=dev)
+    y = torch.empty(n, dtype=torch.uint8, device=dev)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    sh = stream.cuda_stream
+    assert g.gpulz_compress_split(d_in, n, ws, cs, lvl, *ports, caps, pb, sh) == g.GPULZ_OK
+    plen = [int(v) for v in pb.cpu().numpy()]
+    for _ in range(max(args.warmup, 3)):
+        flush.fill_(1)
+        assert g.gpulz_compress_split(d_in, n, ws, cs, lvl, *ports, caps, pb, sh) == g.GPULZ_OK
+        assert g.gpulz_decompress_split(*ports, plen, y, n, sh) == g.GPULZ_OK
+    assert g.gpulz_device_status(sh) == g.GPULZ_OK
+    K = args.steps
+    ev = [tuple(torch.cuda.Event(enable_timing=True) for _ in range(3)) for _ in range(K)]
+    torch.cuda.synchronize()
+    with ClockSampler(0) as clocks:
+        for k in range(K):
+            flush.fill_(k & 0xFF)
+            ev[k][0].record(stream)
+            assert g.gpulz_compress_split(d_in, n, ws, cs, lvl, *ports, caps, pb, sh) == g.GPULZ_OK
+            ev[k][1].record(stream)
+            assert g.gpulz_decompress_split(*ports, plen, y, n, sh) == g.GPULZ_OK
+            ev[k][2].record(stream)
+        torch.cuda.synchronize()
+    t_enc = [a.elapsed_time(b) for a, b, c in ev]
+    t_dec = [b.elapsed_time(c) for a, b, c in ev]
+    status = g.gpulz_device_status(sh)
+    import oracle
+    ref = oracle.compress_split(x, ws, cs, lvl)
+    got = [p[:k].cpu().numpy() for p, k in zip(ports, plen)]
+    ok = all(np.array_equal(a, b) for a, b in zip(got, ref)) and np.array_equal(y.cpu().numpy(), x)
+    enc_ms, dec_ms = statistics.mean(t_enc), statistics.mean(t_dec)
+    total = sum(plen)
+    line = {
+        "metric": "GPULZ split-mode encode+decode round-trip throughput (uncompressed GB/s)",
+        "value": round(n * K / ((sum(t_enc) + sum(t_dec)) * 1e-3) / 1e9, 3),
+        "unit": UNIT, "n_gpus": 1, "steps": K, "warmup": max(args.warmup, 3),
+        "ms_per_step": round((sum(t_enc) + sum(t_dec)) / K, 5),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": cfg.dtype,
+        "data": "synthetic (seeded stand-in for Lorenzo-quantized CLDHGH residuals)",
+        "config": dict(workload_config(cfg), format="split (meta, literals, lengths, offsets)"),
+        "encode_gbs": round(n / (enc_ms * 1e-3) / 1e9, 2),
+        "decode_gbs": round(n / (dec_ms * 1e-3) / 1e9, 2),
+        "port_bytes": dict(zip(("meta", "literals", "lengths", "offsets"), plen)),
+        "ratio": round(n / total, 4),
+        "parity": "bit-exact vs oracle" if ok and status == 0 else "MISMATCH",
+        "device_status": status,
+        "gpu_launches": 5 * K,
+        "clocks": clocks.summary(),
+    }
+    print(json.dumps(line), flush=True)
+
+
 def main():
     args = parse_args()
     if args.impl == "reference":
         run_reference(args)
+    elif args.split:
+        run_split(args)
     else:
         run_ours(args)
 
