@@ -819,16 +819,30 @@ __global__ void __launch_bounds__(kScanThreads) offsets_pass_split(EncodeArgs a,
     }
 }
 
+// Copy n bytes from a slot to a port at any byte offset: the head bytes up
+// to a 4-byte boundary of the destination, then 32-bit stores of words
+// assembled from two aligned slot words (a funnel shift), then the tail
+// bytes; nothing at or past cap. The slot reads are aligned words that each
+// hold at least one of the n bytes, so they stay inside the slot area (a
+// multiple of 4 bytes long).
 __device__ __forceinline__ void copy_bytes_capped(uint8_t* dst, uint64_t at, uint64_t cap,
                                                   const uint8_t* src, uint32_t n, int lane) {
-    if (((at | n | reinterpret_cast<uintptr_t>(src) | reinterpret_cast<uintptr_t>(dst)) & 3u) == 0) {
-        for (uint32_t i = 4u * lane; i < n; i += 128u)
-            if (at + i + 4 <= cap)
-                *reinterpret_cast<uint32_t*>(dst + at + i) = *reinterpret_cast<const uint32_t*>(src + i);
-    } else {
-        for (uint32_t i = lane; i < n; i += 32u)
-            if (at + i < cap) dst[at + i] = src[i];
+    const uint32_t mis = (uint32_t)(reinterpret_cast<uintptr_t>(dst + at) & 3u);
+    const uint32_t head = mis == 0u ? 0u : (4u - mis < n ? 4u - mis : n);
+    if ((uint32_t)lane < head && at + lane < cap) dst[at + lane] = src[lane];
+    const uint32_t nw = (n - head) / 4u;
+    const uint8_t* s0 = src + head;
+    const uint32_t sh = (uint32_t)(reinterpret_cast<uintptr_t>(s0) & 3u);
+    const uint32_t* sw = reinterpret_cast<const uint32_t*>(s0 - sh);
+    uint32_t* dw = reinterpret_cast<uint32_t*>(dst + at + head);
+    for (uint32_t i = lane; i < nw; i += 32u) {
+        // the second word is needed only when shifting (no read past the bytes otherwise)
+        const uint32_t i2 = sh == 0u ? i : i + 1u;
+        const uint32_t v = __funnelshift_r(sw[i], sw[i2], 8u * sh);
+        if (at + head + 4ull * i + 4 <= cap) dw[i] = v;
     }
+    const uint32_t done = head + 4u * nw;
+    if ((uint32_t)lane < n - done && at + done + lane < cap) dst[at + done + lane] = src[done + lane];
 }
 
 __global__ void __launch_bounds__(kCopyWarps * 32) copy_pass_split(EncodeArgs a) {
