@@ -62,8 +62,7 @@ def dist_env():
 def workload_config(cfg):
     return {
         "workload": cfg.name,
-        "field": "x".join(str(s) for s in cfg.shape) + " float32 sinusoids+noise, "
-                 + cfg.lorenzo + " Lorenzo codes (" + cfg.dtype + ", radius %d)" % cfg.radius,
+        "field": "x".join(str(s) for s in cfg.shape) + " float32 sinusoids+noise, " + cfg.codes,
         "n_bytes": cfg.n_bytes,
         "word_size": cfg.word_size,
         "chunk_size": cfg.chunk_size,

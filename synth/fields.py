@@ -17,6 +17,11 @@ each workload is a synthetic field of the same shape and code distribution:
   with zero outside (2D: 4-term, 3D: 8-term inclusion-exclusion; the byte
   workload applies 2D per z-slice); ``code = clamp(delta + R, 0, 2R - 1)``.
 * layout: row-major, x fastest; volumes z-major.
+* sparse workload (mostly-zero codes, the zero-chunk path at scale): the same
+  2D field, quantized as ``q = round(max(x - t, 0) / (2 eb))`` with the
+  threshold ``t`` at 90 % of the noisy field's range, stored as u16; only the
+  sinusoid crests are nonzero (about 0.1 % of the codes; about 70 % of
+  the 2 KB chunks are all zero).
 
 Everything is deterministic in the seed (numpy PCG64).
 """
@@ -33,10 +38,10 @@ class Config:
     name: str
     shape: tuple            # (ny, nx) or (nz, ny, nx)
     directions: int         # 2 or 3 (dimension of the sinusoid directions)
-    lorenzo: str            # "2d", "3d" or "2d_per_slice"
+    lorenzo: str            # "2d", "3d", "2d_per_slice" or "sparse"
     eb_rel: float
     radius: int
-    dtype: str              # "u32" or "u8"
+    dtype: str              # "u32", "u16" or "u8"
     chunk_size: int
     word_size: int
     match_level: int
@@ -44,18 +49,24 @@ class Config:
 
     @property
     def n_bytes(self) -> int:
-        return int(np.prod(self.shape)) * (4 if self.dtype == "u32" else 1)
+        return int(np.prod(self.shape)) * {"u32": 4, "u16": 2, "u8": 1}[self.dtype]
+
+    @property
+    def codes(self) -> str:
+        if self.lorenzo == "sparse":
+            return "thresholded crest codes (%s, 90%% of range)" % self.dtype
+        return "%s Lorenzo codes (%s, radius %d)" % (self.lorenzo, self.dtype, self.radius)
 
     def describe(self) -> str:
         dims = "x".join(str(s) for s in self.shape)
-        return ("%s %s float32 field -> %s Lorenzo codes (%s, R=%d), chunk_size=%d, "
-                "word_size=%d, match_level=%d" % (self.name, dims, self.lorenzo, self.dtype,
-                                                  self.radius, self.chunk_size, self.word_size,
-                                                  self.match_level))
+        return ("%s %s float32 field -> %s, chunk_size=%d, word_size=%d, match_level=%d"
+                % (self.name, dims, self.codes, self.chunk_size, self.word_size,
+                   self.match_level))
 
 
-# The five workloads: a tiny plane, the 1800x3600 plane at both match levels,
-# a 512^3 volume, and the 1800x3600x16 byte stream.
+# The workloads: a tiny plane, the 1800x3600 plane at both match levels,
+# a 512^3 volume, the 1800x3600x16 byte stream, the plane as u16 codes and a
+# mostly-zero u16 field.
 CONFIGS = {
     1: Config("tiny_256x256_u32", (256, 256), 2, "2d", 1e-3, 32768, "u32", 2048, 4, 0,
               20261202 + 1),
@@ -67,6 +78,12 @@ CONFIGS = {
               1, 20261202 + 4),
     5: Config("bytes_1800x3600x16_u8_l1", (16, 1800, 3600), 3, "2d_per_slice", 1e-2, 128, "u8",
               4096, 1, 1, 20261202 + 5),
+    # word_size 2 (u16 codes, the pages' common pairing with a 16-bit entropy
+    # coder) and a mostly-zero input exercising zero chunks at scale
+    6: Config("plane_1800x3600_u16_l1", (1800, 3600), 2, "2d", 1e-3, 32768, "u16", 4096, 2, 1,
+              20261202 + 6),
+    7: Config("sparse_4096x4096_u16_l0", (4096, 4096), 2, "sparse", 1e-3, 32768, "u16", 2048, 2,
+              0, 20261202 + 7),
 }
 
 
@@ -142,8 +159,12 @@ def lorenzo_codes(field: np.ndarray, cfg: Config) -> np.ndarray:
     eb = cfg.eb_rel * (f64_hi - f64_lo)
     if eb <= 0.0:
         eb = 1.0
-    dt = np.uint32 if cfg.dtype == "u32" else np.uint8
+    dt = {"u32": np.uint32, "u16": np.uint16, "u8": np.uint8}[cfg.dtype]
     R = cfg.radius
+    if cfg.lorenzo == "sparse":
+        t = f64_lo + 0.90 * (f64_hi - f64_lo)
+        q = _round_half_away(np.maximum(field.astype(np.float64) - t, 0.0) / (2.0 * eb))
+        return np.clip(q, 0, 65535).astype(dt)
     if cfg.lorenzo == "2d":
         q = _round_half_away(field.astype(np.float64) / (2.0 * eb))
         delta = _lorenzo_2d(q)

@@ -28,9 +28,9 @@ def _check(orc, x, ws, cs, lvl):
 
 
 # ---------------------------------------------------------------------------
-# the five workloads at full size
+# the seven workloads at full size
 # ---------------------------------------------------------------------------
-@pytest.mark.parametrize("cfg_id", [1, 2, 3, 4, 5])
+@pytest.mark.parametrize("cfg_id", [1, 2, 3, 4, 5, 6, 7])
 def test_workload_full_size(orc, cfg_id):
     import synth
     cfg = synth.CONFIGS[cfg_id]

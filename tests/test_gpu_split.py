@@ -48,7 +48,7 @@ def _check(orc, x, ws, cs, lvl):
     return got
 
 
-@pytest.mark.parametrize("cfg_id", [1, 2, 3, 5])
+@pytest.mark.parametrize("cfg_id", [1, 2, 3, 5, 6, 7])
 def test_split_workloads(orc, cfg_id):
     import synth
     cfg = synth.CONFIGS[cfg_id]

@@ -264,6 +264,30 @@ def test_round_trip_tiny_workload(orc, cfg_id, lvl):
     assert np.array_equal(streamcheck.replay(p), x)
 
 
+def test_sparse_workload_zero_chunks(orc):
+    # the zero-chunk sentinel at workload scale: a chunk is coded {0, 0} exactly
+    # when its bytes are all zero, and the other chunks replay to the input
+    import synth
+    cfg = synth.CONFIGS[7]
+    x = synth.generate(7)[: 4 << 20]
+    s = orc.compress(x, cfg.word_size, cfg.chunk_size, cfg.match_level)
+    p = streamcheck.check_invariants(s, x.size)
+    cs = cfg.chunk_size
+    zero = [not x[i: i + cs].any() for i in range(0, x.size, cs)]
+    assert [ch["kind"] == "zero" for ch in p["chunks"]] == zero
+    assert 0.3 < sum(zero) / len(zero) < 1.0
+    assert np.array_equal(streamcheck.replay(p), x)
+
+
+def test_u16_workload_codes():
+    # word_size 2 workload: Lorenzo codes centred on the radius, within u16
+    import synth
+    cfg = synth.CONFIGS[6]
+    assert (cfg.word_size, cfg.dtype, cfg.radius) == (2, "u16", 32768)
+    v = synth.generate(6)[: 1 << 20].view(np.uint16)
+    assert abs(int(np.median(v)) - cfg.radius) <= 2
+
+
 def test_levels_decode_identically_plane(orc):
     import synth
     x = synth.generate(2)[: 1 << 21]
