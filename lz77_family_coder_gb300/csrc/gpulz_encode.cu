@@ -34,7 +34,7 @@ namespace {
 constexpr uint32_t FULL = 0xFFFFFFFFu;
 
 struct EncLayout {
-    uint32_t el, om, lo, tab, fl, data, misc, total;
+    uint32_t el, om, lo, sa, tab, fl, data, misc, total;
 };
 
 __host__ __device__ inline uint32_t align16(uint32_t v) { return (v + 15u) & ~15u; }
@@ -45,6 +45,7 @@ __host__ __device__ inline EncLayout enc_layout(uint32_t cs, uint32_t E, int lev
     L.el = o;   o = align16(o + cs + E);                 // elements, 16 B pad per 16 elements
     L.om = o;   o = align16(o + 4u * (E + E / 4u));      // omask, 4 pad words per 16 masks
     L.lo = o;   o = align16(o + 2u * E);                 // (len | off << 8) per position
+    L.sa = o;   o = align16(o + E / 2u);                 // AND of each segment's masks (<= E/8 u32)
     L.tab = o;  o = align16(o + (level ? 8u * E : 0u));  // level-1 table, 2E buckets of u32
     L.fl = o;   o = align16(o + E / 8u);                 // flag staging
     L.data = o; o = align16(o + cs + 16u);               // block staging
@@ -203,6 +204,16 @@ __device__ __forceinline__ void near_masks(const uint8_t* s_el, uint32_t base, u
     }
 }
 
+// True when every live chain (bit p of `live`) keeps an offset after AND-ing
+// with `sa`, the AND of the masks of the positions to be skipped.
+template <int SEGP>
+__device__ __forceinline__ bool chains_live(const uint32_t (&cc)[SEGP], uint32_t live, uint32_t sa) {
+    bool all = true;
+#pragma unroll
+    for (int p = 0; p < SEGP; ++p) all = all && (((live >> p) & 1u) == 0u || (cc[p] & sa) != 0u);
+    return all;
+}
+
 // 4 bits -> 4 bytes of 0/1.
 __device__ __forceinline__ uint32_t expand4(uint32_t bits) { return (bits * 0x00204081u) & 0x01010101u; }
 
@@ -223,6 +234,7 @@ __global__ void __launch_bounds__(256, 4) encode_kernel(EncodeArgs a) {
     uint8_t* s_el = smem + L.el;
     uint32_t* s_om = reinterpret_cast<uint32_t*>(smem + L.om);
     uint16_t* s_lo = reinterpret_cast<uint16_t*>(smem + L.lo);
+    uint32_t* s_sa = reinterpret_cast<uint32_t*>(smem + L.sa);
     uint32_t* s_tab = reinterpret_cast<uint32_t*>(smem + L.tab);
     uint32_t* s_fl = reinterpret_cast<uint32_t*>(smem + L.fl);
     uint8_t* s_data = smem + L.data;
@@ -295,9 +307,13 @@ __global__ void __launch_bounds__(256, 4) encode_kernel(EncodeArgs a) {
                 near_masks<WS, SEGP>(s_el, seg_a, m);
                 {
                     uint4* dst = reinterpret_cast<uint4*>(s_om + om_idx(seg_a));
+                    uint32_t sa = m[0];
 #pragma unroll
-                    for (int q = 0; q < SEGP / 4; ++q)
+                    for (int q = 0; q < SEGP / 4; ++q) {
                         dst[q] = make_uint4(m[4 * q], m[4 * q + 1], m[4 * q + 2], m[4 * q + 3]);
+                        sa &= m[4 * q] & m[4 * q + 1] & m[4 * q + 2] & m[4 * q + 3];
+                    }
+                    s_sa[tid] = sa;  // the offsets that match at every position of the segment
                 }
                 __syncthreads();
 
@@ -337,27 +353,60 @@ __global__ void __launch_bounds__(256, 4) encode_kernel(EncodeArgs a) {
                     // Chains still alive at the segment end continue over the
                     // following positions' masks in lockstep: one shared-memory
                     // load per step serves all of them, so a long run costs
-                    // O(run) loads rather than O(run^2).
+                    // O(run) loads rather than O(run^2). Once the chains look
+                    // long (all of them alive, or a whole segment survived),
+                    // four following segments, else one, are taken in one step
+                    // when the AND of their masks keeps every live chain nonzero
+                    // and no chain reaches the length cap in them, so a run of
+                    // one repeated word costs a few steps per thread; otherwise
+                    // (and for the last steps before the cap) the segment goes
+                    // position by position.
                     if (P) {
                         uint32_t A2 = P;
-                        for (uint32_t st = 0; A2 != 0u; ++st) {
-                            const uint32_t q = seg_a + (uint32_t)SEGP + st;
-                            if (q >= E) break;
-                            const uint32_t om = s_om[om_idx(q)];
-                            uint32_t An = 0;
+                        uint32_t st = 0;  // positions taken past the segment end
+                        while (A2 != 0u && seg_a + (uint32_t)SEGP + st < E) {
+                            const uint32_t q0 = seg_a + (uint32_t)SEGP + st;  // a segment start
+                            if (A2 == (1u << SEGP) - 1u || st >= (uint32_t)SEGP) {
+                                const uint32_t j = q0 / (uint32_t)SEGP;
+                                const uint32_t p0 = (uint32_t)__ffs(A2) - 1u;        // longest live chain
+                                const uint32_t room = (uint32_t)kMaxLen - (SEGP - p0 + st);  // steps until p0 is capped
+                                uint32_t take = 0, sa = 0;
+                                if (room > 4u * SEGP && q0 + 4u * SEGP <= E) {
+                                    sa = s_sa[j] & s_sa[j + 1] & s_sa[j + 2] & s_sa[j + 3];
+                                    if (chains_live<SEGP>(cc, A2, sa)) take = 4u * SEGP;
+                                }
+                                if (!take && room > (uint32_t)SEGP) {
+                                    sa = s_sa[j];
+                                    if (chains_live<SEGP>(cc, A2, sa)) take = SEGP;
+                                }
+                                if (take) {
 #pragma unroll
-                            for (int p = 0; p < SEGP; ++p) {
-                                const uint32_t x = cc[p] & om;
-                                const bool ok = ((A2 >> p) & 1u) && x != 0u;
-                                cc[p] = ok ? x : cc[p];
-                                An |= (uint32_t)ok << p;
+                                    for (int p = 0; p < SEGP; ++p)
+                                        if ((A2 >> p) & 1u) cc[p] &= sa;
+#pragma unroll
+                                    for (int w = 0; w < SEGP / 4; ++w)
+                                        lb[w] += take * expand4((A2 >> (4 * w)) & 15u);
+                                    st += take;
+                                    continue;
+                                }
                             }
+                            for (int k = 0; k < SEGP && A2 != 0u; ++k, ++st) {
+                                const uint32_t om = s_om[om_idx(q0 + (uint32_t)k)];
+                                uint32_t An = 0;
 #pragma unroll
-                            for (int w = 0; w < SEGP / 4; ++w) lb[w] += expand4((An >> (4 * w)) & 15u);
-                            // length of chain p is now SEGP - p + st + 1: stop at the cap
-                            const int over = (int)(SEGP + st + 1u) - kMaxLen;
-                            if (over >= 0) An &= ~((2u << (over < SEGP - 1 ? over : SEGP - 1)) - 1u);
-                            A2 = An;
+                                for (int p = 0; p < SEGP; ++p) {
+                                    const uint32_t x = cc[p] & om;
+                                    const bool ok = ((A2 >> p) & 1u) && x != 0u;
+                                    cc[p] = ok ? x : cc[p];
+                                    An |= (uint32_t)ok << p;
+                                }
+#pragma unroll
+                                for (int w = 0; w < SEGP / 4; ++w) lb[w] += expand4((An >> (4 * w)) & 15u);
+                                // length of chain p is now SEGP - p + st + 1: stop at the cap
+                                const int over = (int)(SEGP + st + 1u) - kMaxLen;
+                                if (over >= 0) An &= ~((2u << (over < SEGP - 1 ? over : SEGP - 1)) - 1u);
+                                A2 = An;
+                            }
                         }
                     }
                     uint32_t lw[SEGP / 2];
@@ -470,6 +519,15 @@ __global__ void __launch_bounds__(256, 4) encode_kernel(EncodeArgs a) {
                 // entry (the previous segment's exit) differs from the entry its
                 // path assumed re-walks from it, keeping its old path from the
                 // first common position on. This repeats until no entry changes.
+                // A frontier speeds up long matches: the last thread whose entry
+                // is known exact (thread 0 from the start) and its exit. Every
+                // thread after it whose segment starts at or before that exit
+                // takes the exit as its entry at once (the threads it jumps
+                // over pass it through), so a match spanning many segments costs
+                // one round, not one per segment. It starts in the third round
+                // (most chunks are done after two). The rounds still end only
+                // when no entry changes, which only the sequential parse
+                // satisfies.
                 uint32_t T[4] = {0u, 0u, 0u, 0u};  // step of each position, one byte each
                 {
                     uint32_t lw[8];
@@ -499,11 +557,22 @@ __global__ void __launch_bounds__(256, 4) encode_kernel(EncodeArgs a) {
                     }
                     exit_abs = seg_a + p;
                 }
-                for (;;) {
+                if (tid == 0) s_misc[24] = exit_abs;  // frontier: thread 0, its exit
+                for (uint32_t rnd = 0;; ++rnd) {
                     uint32_t prev = __shfl_up_sync(FULL, exit_abs, 1);
                     if (lane == 31) s_misc[8 + warp] = exit_abs;
                     __syncthreads();
                     if (lane == 0) prev = warp == 0 ? 0u : s_misc[8 + warp - 1];
+                    const bool use_fr = rnd >= 2u;
+                    const uint32_t fb = rnd & 1u;
+                    uint32_t fr = 0, fx = 0;
+                    bool reached = false;
+                    if (use_fr) {
+                        fr = s_misc[24 + fb];
+                        fx = fr & 0xFFFFu;
+                        reached = (uint32_t)tid > (fr >> 16) && seg_a <= fx;
+                        if (reached) prev = fx;
+                    }
                     const uint32_t te = prev - seg_a;  // true entry, relative
                     const bool changed = te != cur_e;
                     if (changed) {
@@ -530,6 +599,14 @@ __global__ void __launch_bounds__(256, 4) encode_kernel(EncodeArgs a) {
                             }
                         }
                         cur_e = te;
+                    }
+                    // the thread whose segment holds the frontier exit now has
+                    // an exact entry and becomes the next frontier
+                    if (use_fr) {
+                        if (reached && fx < seg_a + (uint32_t)SEGP)
+                            s_misc[25 - fb] = ((uint32_t)tid << 16) | exit_abs;
+                        else if (tid == 0 && fx >= E)
+                            s_misc[25 - fb] = fr;
                     }
                     if (!__syncthreads_or(changed)) break;
                 }
