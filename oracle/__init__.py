@@ -68,6 +68,8 @@ def _load():
         lib.orc_compress_bound.restype = ctypes.c_uint64
         lib.orc_near_matches.argtypes = [u32p, ctypes.c_int, u8p, u8p]
         lib.orc_near_matches.restype = None
+        lib.orc_near_matches_w.argtypes = [u32p, ctypes.c_int, ctypes.c_int, u8p, u8p]
+        lib.orc_near_matches_w.restype = None
         lib.orc_level1_matches.argtypes = [u32p, ctypes.c_int, u8p, u8p]
         lib.orc_level1_matches.restype = None
         lib.orc_encode_chunk.argtypes = [u8p, ctypes.c_int, ctypes.c_int, ctypes.c_int, u8p,
@@ -76,12 +78,20 @@ def _load():
         lib.orc_compress.argtypes = [u8p, ctypes.c_uint64, ctypes.c_int, ctypes.c_int,
                                      ctypes.c_int, u8p, ctypes.c_uint64]
         lib.orc_compress.restype = ctypes.c_int64
+        lib.orc_compress_w.argtypes = [u8p, ctypes.c_uint64, ctypes.c_int, ctypes.c_int,
+                                       ctypes.c_int, ctypes.c_int, u8p, ctypes.c_uint64]
+        lib.orc_compress_w.restype = ctypes.c_int64
         lib.orc_decompress.argtypes = [u8p, ctypes.c_uint64, u8p, ctypes.c_uint64]
         lib.orc_decompress.restype = ctypes.c_int
         lib.orc_encode_chunk_range.argtypes = [u8p, ctypes.c_uint64, ctypes.c_int, ctypes.c_int,
                                                ctypes.c_int, ctypes.c_uint64, ctypes.c_uint64,
                                                u8p, u32p, u32p]
         lib.orc_encode_chunk_range.restype = None
+        lib.orc_encode_chunk_range_w.argtypes = [u8p, ctypes.c_uint64, ctypes.c_int,
+                                                 ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                                                 ctypes.c_uint64, ctypes.c_uint64, u8p, u32p,
+                                                 u32p]
+        lib.orc_encode_chunk_range_w.restype = None
         u64p = ctypes.POINTER(ctypes.c_uint64)
         lib.orc_decode_chunk_range.argtypes = [u8p, ctypes.c_uint64, u64p, u8p, ctypes.c_uint64,
                                                ctypes.c_uint64, ctypes.c_uint64]
@@ -126,12 +136,16 @@ def compress_bound(n_bytes: int, word_size: int, chunk_size: int) -> int:
     return _load().orc_compress_bound(n_bytes, word_size, chunk_size)
 
 
-def near_matches(words) -> tuple[np.ndarray, np.ndarray]:
-    """Level-0 (length, offset) for every position of one chunk of words."""
+def near_matches(words, window: int = 32) -> tuple[np.ndarray, np.ndarray]:
+    """Level-0 (length, offset) for every position of one chunk of words, over
+    a near window of `window` elements (32 by default; up to 64)."""
     w = np.ascontiguousarray(np.asarray(words, dtype=np.uint32))
     ln = np.zeros(w.size, np.uint8)
     of = np.zeros(w.size, np.uint8)
-    _load().orc_near_matches(_u32(w), w.size, _u8(ln), _u8(of))
+    if window == 32:
+        _load().orc_near_matches(_u32(w), w.size, _u8(ln), _u8(of))
+    else:
+        _load().orc_near_matches_w(_u32(w), w.size, window, _u8(ln), _u8(of))
     return ln, of
 
 
@@ -156,12 +170,15 @@ def encode_chunk(chunk, word_size: int, chunk_size: int, match_level: int):
     return out[:n].copy(), int(items[0]), int(dbytes[0])
 
 
-def compress(data, word_size: int, chunk_size: int, match_level: int) -> np.ndarray:
-    """Whole-stream encode; returns the stream as a uint8 array."""
+def compress(data, word_size: int, chunk_size: int, match_level: int,
+             window: int = 32) -> np.ndarray:
+    """Whole-stream encode; returns the stream as a uint8 array. `window` is
+    the near window in elements (32 by default, up to 64)."""
     src = _as_bytes(data)
     cap = compress_bound(src.size, word_size, chunk_size)
     out = np.zeros(cap, np.uint8)
-    n = _load().orc_compress(_u8(src), src.size, word_size, chunk_size, match_level, _u8(out), cap)
+    n = _load().orc_compress_w(_u8(src), src.size, word_size, chunk_size, match_level, window,
+                               _u8(out), cap)
     if n < 0:
         raise ValueError("oracle compress failed with code %d" % n)
     return out[:n].copy()
@@ -231,7 +248,7 @@ def decompress_status(stream, n_bytes: int) -> int:
 
 
 def compress_threads(data, word_size: int, chunk_size: int, match_level: int,
-                     threads: int) -> np.ndarray:
+                     threads: int, window: int = 32) -> np.ndarray:
     """The same oracle chunk encoder spread over host threads by chunk range.
 
     Chunks are independent, so concatenating the per-chunk blocks in chunk
@@ -249,9 +266,9 @@ def compress_threads(data, word_size: int, chunk_size: int, match_level: int,
     bounds = [chunks * t // threads for t in range(threads + 1)]
 
     def run(t):
-        lib.orc_encode_chunk_range(_u8(src), n, word_size, chunk_size, match_level,
-                                   bounds[t], bounds[t + 1], _u8(blocks), _u32(sizes),
-                                   _u32(entries))
+        lib.orc_encode_chunk_range_w(_u8(src), n, word_size, chunk_size, match_level, window,
+                                     bounds[t], bounds[t + 1], _u8(blocks), _u32(sizes),
+                                     _u32(entries))
 
     pool = [threading.Thread(target=run, args=(t,)) for t in range(threads)]
     for th in pool:

@@ -17,6 +17,8 @@
  *   exact longest match over the 32-element
  *   near window (omask + AND of successive
  *   masks), length capped at 255             -> stage page, match-search section
+ *   (windows of 33..64 elements for the
+ *   window-width study, same section)
  *   hashed two-word-key long-range candidates
  *   over 8 sub-blocks, offsets to 255,
  *   buckets keep max(pos+1)                  -> stage page, match-search section;
@@ -55,7 +57,8 @@
 #define ORC_RAW_BIT 0x80000000u
 
 /* ---- method constants from the pages ---- */
-#define ORC_NEAR_WINDOW 32 /* fixed 32-element near window */
+#define ORC_NEAR_WINDOW 32 /* default 32-element near window */
+#define ORC_MAX_WINDOW 64  /* widest near window of the window-width study */
 #define ORC_MAX_LEN 255    /* one-byte length field */
 #define ORC_MAX_OFF 255    /* one-byte offset field, "offsets to 255" */
 #define ORC_SUBBLOCKS 8    /* chunk walked in 8 sub-blocks */
@@ -116,23 +119,29 @@ uint64_t orc_compress_bound(uint64_t n_bytes, int word_size, int chunk_size) {
 }
 
 /* ------------------------------------------------------------------------ */
-/* Level 0: exact longest match over the 32-element near window.            */
+/* Level 0: exact longest match over the near window (32 elements; 33..64   */
+/* for the window-width study of the match-search section).                 */
 /* ------------------------------------------------------------------------ */
 void orc_near_matches(const uint32_t* w, int elems, uint8_t* len_out, uint8_t* off_out) {
-    uint32_t* omask = (uint32_t*)malloc(sizeof(uint32_t) * (size_t)elems);
-    /* omask[i] bit (o-1) set iff w[i] == w[i-o], 1 <= o <= 32, i-o >= 0. */
+    orc_near_matches_w(w, elems, ORC_NEAR_WINDOW, len_out, off_out);
+}
+
+void orc_near_matches_w(const uint32_t* w, int elems, int window, uint8_t* len_out,
+                        uint8_t* off_out) {
+    uint64_t* omask = (uint64_t*)malloc(sizeof(uint64_t) * (size_t)elems);
+    /* omask[i] bit (o-1) set iff w[i] == w[i-o], 1 <= o <= window, i-o >= 0. */
     for (int i = 0; i < elems; ++i) {
-        uint32_t m = 0;
-        for (int o = 1; o <= ORC_NEAR_WINDOW; ++o) {
+        uint64_t m = 0;
+        for (int o = 1; o <= window; ++o) {
             if (i - o < 0) break;
-            if (w[i] == w[i - o]) m |= 1u << (o - 1);
+            if (w[i] == w[i - o]) m |= 1ull << (o - 1);
         }
         omask[i] = m;
     }
     /* AND successive masks: the surviving offsets after k steps are exactly
      * those that match for k consecutive elements. */
     for (int i = 0; i < elems; ++i) {
-        uint32_t m = omask[i];
+        uint64_t m = omask[i];
         if (m == 0) {
             len_out[i] = 0;
             off_out[i] = 0;
@@ -142,14 +151,14 @@ void orc_near_matches(const uint32_t* w, int elems, uint8_t* len_out, uint8_t* o
         if (cap > ORC_MAX_LEN) cap = ORC_MAX_LEN;
         int len = 1;
         while (len < cap) {
-            uint32_t next = m & omask[i + len];
+            uint64_t next = m & omask[i + len];
             if (next == 0) break;
             m = next;
             ++len;
         }
         /* nearest surviving offset */
         int off = 1;
-        while (((m >> (off - 1)) & 1u) == 0) ++off;
+        while (((m >> (off - 1)) & 1ull) == 0) ++off;
         len_out[i] = (uint8_t)len;
         off_out[i] = (uint8_t)off;
     }
@@ -212,6 +221,13 @@ static uint32_t load_word(const uint8_t* p, int ws) {
  * the block's byte length. */
 uint32_t orc_encode_chunk(const uint8_t* chunk, int word_size, int chunk_size, int match_level,
                           uint8_t* block_out, uint32_t* entry_items, uint32_t* entry_data) {
+    return orc_encode_chunk_w(chunk, word_size, chunk_size, match_level, ORC_NEAR_WINDOW,
+                              block_out, entry_items, entry_data);
+}
+
+uint32_t orc_encode_chunk_w(const uint8_t* chunk, int word_size, int chunk_size, int match_level,
+                            int window, uint8_t* block_out, uint32_t* entry_items,
+                            uint32_t* entry_data) {
     int elems = chunk_size / word_size;
 
     /* zero-chunk sentinel */
@@ -232,7 +248,7 @@ uint32_t orc_encode_chunk(const uint8_t* chunk, int word_size, int chunk_size, i
     for (int i = 0; i < elems; ++i) w[i] = load_word(chunk + (size_t)i * word_size, word_size);
     uint8_t* len = (uint8_t*)malloc((size_t)elems);
     uint8_t* off = (uint8_t*)malloc((size_t)elems);
-    orc_near_matches(w, elems, len, off);
+    orc_near_matches_w(w, elems, window, len, off);
     if (match_level == 1) orc_level1_matches(w, elems, len, off);
 
     /* greedy sequential parse */
@@ -285,8 +301,15 @@ uint32_t orc_encode_chunk(const uint8_t* chunk, int word_size, int chunk_size, i
 /* ------------------------------------------------------------------------ */
 int64_t orc_compress(const uint8_t* in, uint64_t n_bytes, int word_size, int chunk_size,
                      int match_level, uint8_t* out, uint64_t capacity) {
+    return orc_compress_w(in, n_bytes, word_size, chunk_size, match_level, ORC_NEAR_WINDOW, out,
+                          capacity);
+}
+
+int64_t orc_compress_w(const uint8_t* in, uint64_t n_bytes, int word_size, int chunk_size,
+                       int match_level, int window, uint8_t* out, uint64_t capacity) {
     if (!orc_valid_geometry(word_size, chunk_size)) return ORC_ERR_INVALID_ARG;
     if (match_level != 0 && match_level != 1) return ORC_ERR_INVALID_ARG;
+    if (window < 1 || window > ORC_MAX_WINDOW) return ORC_ERR_INVALID_ARG;
     if (n_bytes > 0 && in == NULL) return ORC_ERR_INVALID_ARG;
     uint64_t chunks = (n_bytes + (uint64_t)chunk_size - 1) / (uint64_t)chunk_size;
     if (chunks > 0xFFFFFFFFull) return ORC_ERR_INVALID_ARG;
@@ -303,8 +326,8 @@ int64_t orc_compress(const uint8_t* in, uint64_t n_bytes, int word_size, int chu
         memset(chunk, 0, (size_t)chunk_size);
         memcpy(chunk, in + begin, (size_t)take);
         uint32_t items = 0, dbytes = 0;
-        uint32_t blk = orc_encode_chunk(chunk, word_size, chunk_size, match_level, out + pos,
-                                        &items, &dbytes);
+        uint32_t blk = orc_encode_chunk_w(chunk, word_size, chunk_size, match_level, window,
+                                          out + pos, &items, &dbytes);
         put_u32(out + table_at + ORC_ENTRY_BYTES * c, items);
         put_u32(out + table_at + ORC_ENTRY_BYTES * c + 4, dbytes);
         pos += blk;
@@ -435,6 +458,14 @@ int orc_decompress(const uint8_t* in, uint64_t in_len, uint8_t* out, uint64_t n_
 void orc_encode_chunk_range(const uint8_t* in, uint64_t n_bytes, int word_size, int chunk_size,
                             int match_level, uint64_t c0, uint64_t c1, uint8_t* out_blocks,
                             uint32_t* block_bytes, uint32_t* entries) {
+    orc_encode_chunk_range_w(in, n_bytes, word_size, chunk_size, match_level, ORC_NEAR_WINDOW,
+                             c0, c1, out_blocks, block_bytes, entries);
+}
+
+void orc_encode_chunk_range_w(const uint8_t* in, uint64_t n_bytes, int word_size,
+                              int chunk_size, int match_level, int window, uint64_t c0,
+                              uint64_t c1, uint8_t* out_blocks, uint32_t* block_bytes,
+                              uint32_t* entries) {
     uint8_t* chunk = (uint8_t*)malloc((size_t)chunk_size);
     for (uint64_t c = c0; c < c1; ++c) {
         uint64_t begin = c * (uint64_t)chunk_size;
@@ -442,9 +473,9 @@ void orc_encode_chunk_range(const uint8_t* in, uint64_t n_bytes, int word_size, 
         if (take > (uint64_t)chunk_size) take = (uint64_t)chunk_size;
         memset(chunk, 0, (size_t)chunk_size);
         memcpy(chunk, in + begin, (size_t)take);
-        block_bytes[c] = orc_encode_chunk(chunk, word_size, chunk_size, match_level,
-                                          out_blocks + c * (uint64_t)chunk_size, &entries[2 * c],
-                                          &entries[2 * c + 1]);
+        block_bytes[c] = orc_encode_chunk_w(chunk, word_size, chunk_size, match_level, window,
+                                            out_blocks + c * (uint64_t)chunk_size,
+                                            &entries[2 * c], &entries[2 * c + 1]);
     }
     free(chunk);
 }

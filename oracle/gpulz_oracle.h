@@ -26,15 +26,24 @@ uint64_t orc_compress_bound(uint64_t n_bytes, int word_size, int chunk_size);
 /* Per-position longest match of one chunk of `elems` words (zero-extended to
  * 32 bits). len = 0 means no candidate; off is in elements. */
 void orc_near_matches(const uint32_t* w, int elems, uint8_t* len_out, uint8_t* off_out);
+/* Same with a near window of `window` elements (1..64); the default is 32.
+ * The window-width study of the match-search section compares 32, 48, 64. */
+void orc_near_matches_w(const uint32_t* w, int elems, int window, uint8_t* len_out,
+                        uint8_t* off_out);
 void orc_level1_matches(const uint32_t* w, int elems, uint8_t* len_io, uint8_t* off_io);
 
 uint32_t orc_encode_chunk(const uint8_t* chunk, int word_size, int chunk_size, int match_level,
                           uint8_t* block_out, uint32_t* entry_items, uint32_t* entry_data);
+uint32_t orc_encode_chunk_w(const uint8_t* chunk, int word_size, int chunk_size, int match_level,
+                            int window, uint8_t* block_out, uint32_t* entry_items,
+                            uint32_t* entry_data);
 
 /* Returns the stream length, or a negative ORC_ERR_* code. `capacity` must be
  * at least orc_compress_bound(). */
 int64_t orc_compress(const uint8_t* in, uint64_t n_bytes, int word_size, int chunk_size,
                      int match_level, uint8_t* out, uint64_t capacity);
+int64_t orc_compress_w(const uint8_t* in, uint64_t n_bytes, int word_size, int chunk_size,
+                       int match_level, int window, uint8_t* out, uint64_t capacity);
 int orc_parse_header(const uint8_t* in, uint64_t in_len, int* word_size, int* chunk_size,
                      uint64_t* n_chunks, uint64_t* orig_bytes, uint64_t* stream_bytes);
 /* Returns 0, or a negative ORC_ERR_* code. */
@@ -43,6 +52,10 @@ int orc_decompress(const uint8_t* in, uint64_t in_len, uint8_t* out, uint64_t n_
 void orc_encode_chunk_range(const uint8_t* in, uint64_t n_bytes, int word_size, int chunk_size,
                             int match_level, uint64_t c0, uint64_t c1, uint8_t* out_blocks,
                             uint32_t* block_bytes, uint32_t* entries);
+void orc_encode_chunk_range_w(const uint8_t* in, uint64_t n_bytes, int word_size,
+                              int chunk_size, int match_level, int window, uint64_t c0,
+                              uint64_t c1, uint8_t* out_blocks, uint32_t* block_bytes,
+                              uint32_t* entries);
 
 int orc_decode_chunk_range(const uint8_t* in, uint64_t in_len, const uint64_t* block_off,
                            uint8_t* out, uint64_t n_bytes, uint64_t c0, uint64_t c1);

@@ -27,16 +27,17 @@ import streamcheck
 # ----------------------------------------------------------------------------
 # brute force longest match over the near window
 # ----------------------------------------------------------------------------
-def brute_near(w):
+def brute_near(w, window=32):
     """Direct definition: for each i, the longest run w[i+k] == w[i+k-o] over
-    1 <= o <= min(32, i), capped at min(255, E - i); the smallest o wins ties."""
+    1 <= o <= min(window, i), capped at min(255, E - i); the smallest o wins
+    ties."""
     E = len(w)
     L = np.zeros(E, np.uint8)
     O = np.zeros(E, np.uint8)
     for i in range(E):
         cap = min(255, E - i)
         best, bo = 0, 0
-        for o in range(1, min(32, i) + 1):
+        for o in range(1, min(window, i) + 1):
             k = 0
             while k < cap and w[i + k] == w[i + k - o]:
                 k += 1
@@ -73,6 +74,73 @@ def test_near_window_is_32(orc):
         L, _ = orc.near_matches(w)
         assert bool(L[p:].any()) is expect
         assert not L[:p].any()
+
+
+# ----------------------------------------------------------------------------
+# the window-width study (match-search section: 32, 48 and 64 elements)
+# ----------------------------------------------------------------------------
+@pytest.mark.parametrize("window", [1, 17, 33, 48, 63, 64])
+def test_near_random_small_alphabet_window(orc, window):
+    rng = np.random.default_rng(4000 + window)
+    for E in (70, 200):
+        for alphabet in (2, 5, 60):
+            w = rng.integers(0, alphabet, E).astype(np.uint32) * 0x01010101
+            L, O = orc.near_matches(w, window)
+            bl, bo = brute_near(list(w), window)
+            assert np.array_equal(L, bl) and np.array_equal(O, bo), (E, alphabet)
+
+
+@pytest.mark.parametrize("window", [48, 64])
+def test_near_window_bound(orc, window):
+    # period `window` is seen, period `window + 1` is not
+    base = goldens.distinct_u32(window + 1)
+    for p, expect in ((window, True), (window + 1, False)):
+        w = np.tile(base[:p], 1200 // p + 1)[:1200]
+        L, O = orc.near_matches(w, window)
+        assert bool(L[p:].any()) is expect
+        assert not L[:p].any()
+        if expect:
+            assert (O[p:] == p).all()
+
+
+@pytest.mark.parametrize("p", [33, 40, 48, 64])
+def test_period_p_wide_window_closed_form(orc, p):
+    # the level-0 closed form of a period-p chunk holds for p up to the window
+    E = 512
+    w = np.tile(goldens.distinct_u32(p), E // p + 1)[:E]
+    s = orc.compress(w.view(np.uint8), 4, 2048, 0, window=64)
+    toks = streamcheck.parse(s)["chunks"][0]["items"]
+    n_match = -(-(E - p) // 255)
+    assert [t[0] for t in toks] == ["L"] * p + ["M"] * n_match
+    assert [t[1] for t in toks[p:]] == [255] * (n_match - 1) + [E - p - 255 * (n_match - 1)]
+    assert all(t[2] == p for t in toks[p:])
+    # a 32-element window sees none of it
+    s32 = orc.compress(w.view(np.uint8), 4, 2048, 0)
+    assert s32[32 + 8:].size >= 2048
+
+
+@pytest.mark.parametrize("ws,cs", [(4, 2048), (2, 1024), (1, 4096)])
+def test_window_streams_valid(orc, ws, cs):
+    import synth
+    x = synth.generate(2)[: 300_000 + 5]
+    s32 = orc.compress(x, ws, cs, 0)
+    assert np.array_equal(orc.compress(x, ws, cs, 0, window=32), s32)
+    for window in (48, 64):
+        s = orc.compress(x, ws, cs, 0, window=window)
+        p = streamcheck.check_invariants(s, x.size)
+        offs = [t[2] for ch in p["chunks"] for t in ch["items"] if t[0] == "M"]
+        assert max(offs) <= window
+        assert np.array_equal(streamcheck.replay(p), x)
+        assert np.array_equal(orc.decompress(s, x.size), x)
+
+
+def test_window_ratio_climbs_on_plane(orc):
+    # the pages report the level-0 ratio climbing with the window (32 -> 48 -> 64);
+    # on the plane workload the streams shrink in the same order
+    import synth
+    x = synth.generate(2)[: 1 << 21]
+    sizes = [orc.compress(x, 4, 2048, 0, window=w).size for w in (32, 48, 64)]
+    assert sizes[0] > sizes[1] > sizes[2]
 
 
 def test_near_length_cap_and_chunk_end(orc):
