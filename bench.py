@@ -47,6 +47,8 @@ def parse_args():
     p.add_argument("--config", type=int, default=CFG_ID)
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-e2e", action="store_true")
+    p.add_argument("--window", type=int, default=32,
+                   help="exact near window in elements (32..64; above 32 on level-0 workloads)")
     p.add_argument("--split", action="store_true",
                    help="time split mode (four ports) instead of the single stream; one GPU")
     return p.parse_args()
@@ -59,8 +61,9 @@ def dist_env():
     return world, rank, local
 
 
-def workload_config(cfg):
-    return {
+def workload_config(cfg, window=32):
+    extra = {} if window == 32 else {"near_window": window}
+    return extra | {
         "workload": cfg.name,
         "field": "x".join(str(s) for s in cfg.shape) + " float32 sinusoids+noise, " + cfg.codes,
         "n_bytes": cfg.n_bytes,
@@ -194,13 +197,14 @@ def max_over_ranks(value: float, dist, device) -> float:
     return float(t.item())
 
 
-def cpu_baseline(x, cfg, reps=3):
+def cpu_baseline(x, cfg, reps=3, window=32):
     import oracle
     threads = os.cpu_count() or 1
     times = []
     for _ in range(reps):
         t0 = time.perf_counter()
-        s = oracle.compress_threads(x, cfg.word_size, cfg.chunk_size, cfg.match_level, threads)
+        s = oracle.compress_threads(x, cfg.word_size, cfg.chunk_size, cfg.match_level, threads,
+                                    window=window)
         y = oracle.decompress_threads(s, x.size, threads)
         times.append(time.perf_counter() - t0)
     assert (y == x).all()
@@ -240,9 +244,15 @@ def run_ours(args):
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream(dev)
     sh = stream.cuda_stream
+    W = args.window
+
+    def compress_call():
+        if W == 32:
+            return g.gpulz_compress(d_in, n, ws, cs, lvl, out, cap, nb, sh)
+        return g.gpulz_compress_window(d_in, n, ws, cs, lvl, W, out, cap, nb, sh)
 
     def step():
-        st = g.gpulz_compress(d_in, n, ws, cs, lvl, out, cap, nb, sh)
+        st = compress_call()
         assert st == g.GPULZ_OK, st
         st = g.gpulz_decompress(out, y, n, sh)
         assert st == g.GPULZ_OK, st
@@ -270,7 +280,7 @@ def run_ours(args):
         for k in range(K):
             flush.fill_(k & 0xFF)  # evict the input from L2 (outside the events)
             ev[k][0].record(stream)
-            assert g.gpulz_compress(d_in, n, ws, cs, lvl, out, cap, nb, sh) == g.GPULZ_OK
+            assert compress_call() == g.GPULZ_OK
             ev[k][1].record(stream)
             assert g.gpulz_decompress(out, y, n, sh) == g.GPULZ_OK
             ev[k][2].record(stream)
@@ -285,7 +295,7 @@ def run_ours(args):
     for k in range(K):
         flush.fill_(k & 0xFF)
         g.gpulz_set_kernel_events(kev[k][0], kev[k][1])
-        assert g.gpulz_compress(d_in, n, ws, cs, lvl, out, cap, nb, sh) == g.GPULZ_OK
+        assert compress_call() == g.GPULZ_OK
         g.gpulz_set_kernel_events(kev[k][2], kev[k][3])
         assert g.gpulz_decompress(out, y, n, sh) == g.GPULZ_OK
     g.gpulz_set_kernel_events(None, None)
@@ -303,7 +313,7 @@ def run_ours(args):
     parity = "unchecked"
     if rank == 0:
         import oracle
-        ref = oracle.compress_threads(x, ws, cs, lvl, os.cpu_count() or 1)
+        ref = oracle.compress_threads(x, ws, cs, lvl, os.cpu_count() or 1, window=W)
         ok = np.array_equal(stream_host, ref) and np.array_equal(y.cpu().numpy(), x)
         parity = "bit-exact vs oracle" if ok and status == 0 else "MISMATCH"
 
@@ -318,7 +328,7 @@ def run_ours(args):
 
         def e2e_step():
             d_in.copy_(h_x, non_blocking=True)
-            assert g.gpulz_compress(d_in, n, ws, cs, lvl, out, cap, nb, sh) == g.GPULZ_OK
+            assert compress_call() == g.GPULZ_OK
             h_nb.copy_(nb, non_blocking=True)
             stream.synchronize()
             s_len = int(h_nb[0])
@@ -359,7 +369,7 @@ def run_ours(args):
     peak, peak_kind = measured_peak()
     alu_peak, alu_src = alu_peak_tops(dev)
     elems = n // ws
-    enc_ops = 32 * elems  # near-window equality compares: 32 per element
+    enc_ops = W * elems  # near-window equality compares: one per element and offset
     enc_alg = n + S       # bytes: input read + blocks written (to their slots)
     dec_alg = S + n       # bytes: stream read + output written
     enc_s, dec_s = enc_k_ms * 1e-3, dec_k_ms * 1e-3
@@ -398,7 +408,7 @@ def run_ours(args):
         "vs_baseline": None,
         "dtype": cfg.dtype,
         "data": "synthetic (seeded stand-in for Lorenzo-quantized CLDHGH residuals)",
-        "config": workload_config(cfg),
+        "config": workload_config(cfg, W),
         "encode_gbs": round(n / (enc_ms * 1e-3) / 1e9, 2),
         "decode_gbs": round(n / (dec_ms * 1e-3) / 1e9, 2),
         "ratio": round(n / S, 4),
@@ -411,7 +421,7 @@ def run_ours(args):
         "e2e": e2e,
     }
     if not args.no_cpu_baseline and world == 1:
-        line["cpu_baseline"] = cpu_baseline(x, cfg)
+        line["cpu_baseline"] = cpu_baseline(x, cfg, window=W)
     print(json.dumps(line), flush=True)
     if world > 1:
         dist.destroy_process_group()
@@ -431,7 +441,8 @@ def run_reference(args):
     threads = os.cpu_count() or 1
 
     def step():
-        s = oracle.compress_threads(x, cfg.word_size, cfg.chunk_size, cfg.match_level, threads)
+        s = oracle.compress_threads(x, cfg.word_size, cfg.chunk_size, cfg.match_level, threads,
+                                    window=args.window)
         y = oracle.decompress_threads(s, x.size, threads)
         return s, y
 
@@ -459,7 +470,7 @@ def run_reference(args):
         "vs_baseline": None,
         "dtype": cfg.dtype,
         "data": "synthetic (seeded stand-in for Lorenzo-quantized CLDHGH residuals)",
-        "config": workload_config(cfg),
+        "config": workload_config(cfg, args.window),
         "ratio": round(x.size / s.size, 4),
         "cpu_baseline": {"value": value, "unit": UNIT, "cores": threads, "kind": "oracle",
                          "sample": "whole workload per step (%d bytes), encode+decode round trip"
@@ -542,8 +553,16 @@ def run_split(args):
     print(json.dumps(line), flush=True)
 
 
+def synth_level(cfg_id):
+    import synth
+    return synth.CONFIGS[cfg_id].match_level
+
+
 def main():
     args = parse_args()
+    if args.window != 32 and (args.window < 32 or args.window > 64 or args.split or
+                              synth_level(args.config) != 0):
+        raise SystemExit("--window: 32..64, single-stream level-0 workloads only")
     if args.impl == "reference":
         run_reference(args)
     elif args.split:

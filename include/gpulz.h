@@ -92,6 +92,25 @@ gpulz_status gpulz_compress(const void* d_in, size_t n_bytes, int word_size, int
                             cudaStream_t stream);
 
 /*
+ * gpulz_compress_window -- gpulz_compress with a wider exact near window.
+ * (GPULZ stage page, match-search section: the window-width measurement,
+ * ratio at 32, 48 and 64 elements.)
+ *
+ *   window      32..64: the level-0 search finds the longest run over offsets
+ *               1..window (nearest offset on ties), lengths capped at 255 and
+ *               at the chunk end. 32 is gpulz_compress exactly. Above 32,
+ *               match_level must be 0. Offsets still fit the token's byte, so
+ *               the stream format and gpulz_decompress are unchanged.
+ *   Other arguments, ownership and errors as gpulz_compress; a window outside
+ *   32..64, or above 32 with match_level 1, returns GPULZ_ERR_INVALID_ARG and
+ *   launches nothing. A wider window costs a second mask-and-chain pass per
+ *   chunk (about twice the match-search work).
+ */
+gpulz_status gpulz_compress_window(const void* d_in, size_t n_bytes, int word_size,
+                                   int chunk_size, int match_level, int window, void* d_out,
+                                   size_t capacity, size_t* d_out_bytes, cudaStream_t stream);
+
+/*
  * gpulz_decompress -- decode the GPULZ stream at d_in into n_bytes at d_out.
  * (GPULZ stage page: decode paragraph -- one scan recovers every item's
  * offset, each element points back to q - offset, pointer jumping for

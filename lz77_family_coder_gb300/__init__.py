@@ -17,7 +17,8 @@ import os
 __all__ = [
     "GPULZ_OK", "GPULZ_ERR_INVALID_ARG", "GPULZ_ERR_CAPACITY", "GPULZ_ERR_CORRUPT",
     "GPULZ_ERR_TIMEOUT", "GPULZ_ERR_CUDA", "GPULZ_ERR_SIZE_MISMATCH", "GpulzError",
-    "library_path", "load", "build", "gpulz_compress", "gpulz_compress_noalloc", "gpulz_decompress",
+    "library_path", "load", "build", "gpulz_compress", "gpulz_compress_window",
+    "gpulz_compress_noalloc", "gpulz_decompress",
     "gpulz_decompress_bounded", "gpulz_compress_bound", "gpulz_stream_info",
     "gpulz_device_status", "gpulz_set_kernel_events", "gpulz_status_string", "compress",
     "decompress", "gpulz_split_bounds", "gpulz_compress_split", "gpulz_decompress_split",
@@ -64,6 +65,8 @@ def load():
     vp, sz, i32 = ctypes.c_void_p, ctypes.c_size_t, ctypes.c_int
     lib.gpulz_compress.argtypes = [vp, sz, i32, i32, i32, vp, sz, vp, vp]
     lib.gpulz_compress.restype = i32
+    lib.gpulz_compress_window.argtypes = [vp, sz, i32, i32, i32, i32, vp, sz, vp, vp]
+    lib.gpulz_compress_window.restype = i32
     lib.gpulz_compress_noalloc.argtypes = [vp, sz, i32, i32, i32, vp, sz, vp, vp]
     lib.gpulz_compress_noalloc.restype = i32
     lib.gpulz_decompress.argtypes = [vp, vp, sz, vp]
@@ -121,6 +124,13 @@ def gpulz_compress(d_in, n_bytes, word_size, chunk_size, match_level, d_out, cap
                    d_out_bytes, stream=None) -> int:
     return load().gpulz_compress(_ptr(d_in), n_bytes, word_size, chunk_size, match_level,
                                  _ptr(d_out), capacity, _ptr(d_out_bytes), _stream(stream))
+
+
+def gpulz_compress_window(d_in, n_bytes, word_size, chunk_size, match_level, window, d_out,
+                          capacity, d_out_bytes, stream=None) -> int:
+    return load().gpulz_compress_window(_ptr(d_in), n_bytes, word_size, chunk_size, match_level,
+                                        window, _ptr(d_out), capacity, _ptr(d_out_bytes),
+                                        _stream(stream))
 
 
 def gpulz_compress_noalloc(d_in, n_bytes, word_size, chunk_size, match_level, d_out, capacity,
@@ -199,10 +209,11 @@ def gpulz_status_string(status: int) -> str:
 
 # ---- conveniences (torch allocates, the library computes) ----
 def compress(x, word_size: int, chunk_size: int, match_level: int, stream=None, out=None,
-             out_bytes=None):
+             out_bytes=None, window: int = 32):
     """Encode a contiguous CUDA tensor's bytes. Returns (out, out_bytes) tensors:
     ``out`` has compress-bound capacity; ``out_bytes`` (int64, 1 element) holds
-    the stream length on the device (no host synchronisation)."""
+    the stream length on the device (no host synchronisation). ``window`` is
+    the exact near window in elements (32..64; above 32, level 0 only)."""
     import torch
     n = x.numel() * x.element_size()
     cap = gpulz_compress_bound(n, word_size, chunk_size)
@@ -212,8 +223,12 @@ def compress(x, word_size: int, chunk_size: int, match_level: int, stream=None, 
         out = torch.empty(cap, dtype=torch.uint8, device=x.device)
     if out_bytes is None:
         out_bytes = torch.empty(1, dtype=torch.int64, device=x.device)
-    st = gpulz_compress(x if n else None, n, word_size, chunk_size, match_level, out,
-                        out.numel(), out_bytes, stream)
+    if window == 32:
+        st = gpulz_compress(x if n else None, n, word_size, chunk_size, match_level, out,
+                            out.numel(), out_bytes, stream)
+    else:
+        st = gpulz_compress_window(x if n else None, n, word_size, chunk_size, match_level,
+                                   window, out, out.numel(), out_bytes, stream)
     if st != GPULZ_OK:
         raise GpulzError(st, "gpulz_compress")
     return out, out_bytes

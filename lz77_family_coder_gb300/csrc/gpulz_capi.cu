@@ -124,10 +124,12 @@ namespace {
 // Shared by the single-stream and split encoders: argument checks, scratch,
 // and the launch. ports/port_cap are null for the single-stream form.
 gpulz_status compress_impl(const void* d_in, size_t n_bytes, int word_size, int chunk_size,
-                           int match_level, void* d_out, size_t capacity, size_t* d_out_bytes,
-                           uint8_t* const* ports, const size_t* port_cap, cudaStream_t stream) {
+                           int match_level, int window, void* d_out, size_t capacity,
+                           size_t* d_out_bytes, uint8_t* const* ports, const size_t* port_cap,
+                           cudaStream_t stream) {
     if (!valid_geometry(word_size, chunk_size)) return GPULZ_ERR_INVALID_ARG;
     if (match_level != 0 && match_level != 1) return GPULZ_ERR_INVALID_ARG;
+    if (window < 32 || window > 64 || (window > 32 && match_level != 0)) return GPULZ_ERR_INVALID_ARG;
     if ((n_bytes > 0 && d_in == nullptr) || d_out == nullptr || d_out_bytes == nullptr)
         return GPULZ_ERR_INVALID_ARG;
     if (!aligned(d_out, 4) || !aligned(d_out_bytes, 8)) return GPULZ_ERR_INVALID_ARG;
@@ -161,6 +163,7 @@ gpulz_status compress_impl(const void* d_in, size_t n_bytes, int word_size, int 
     a.elems = (uint32_t)(chunk_size / word_size);
     a.n_chunks = (uint32_t)chunks;
     a.hash_bits = log2_exact(2u * a.elems);
+    a.far_mask = window == 32 ? 0u : (window == 64 ? 0xFFFFFFFFu : (1u << (window - 32)) - 1u);
     a.split = ports != nullptr;
     for (int k = 0; k < 3; ++k) {
         a.port[k] = ports ? ports[k] : nullptr;
@@ -175,8 +178,15 @@ gpulz_status compress_impl(const void* d_in, size_t n_bytes, int word_size, int 
 gpulz_status gpulz_compress(const void* d_in, size_t n_bytes, int word_size, int chunk_size,
                             int match_level, void* d_out, size_t capacity, size_t* d_out_bytes,
                             cudaStream_t stream) {
-    return compress_impl(d_in, n_bytes, word_size, chunk_size, match_level, d_out, capacity,
+    return compress_impl(d_in, n_bytes, word_size, chunk_size, match_level, 32, d_out, capacity,
                          d_out_bytes, nullptr, nullptr, stream);
+}
+
+gpulz_status gpulz_compress_window(const void* d_in, size_t n_bytes, int word_size,
+                                   int chunk_size, int match_level, int window, void* d_out,
+                                   size_t capacity, size_t* d_out_bytes, cudaStream_t stream) {
+    return compress_impl(d_in, n_bytes, word_size, chunk_size, match_level, window, d_out,
+                         capacity, d_out_bytes, nullptr, nullptr, stream);
 }
 
 gpulz_status gpulz_split_bounds(size_t n_bytes, int word_size, int chunk_size, size_t bounds[4]) {
@@ -198,8 +208,8 @@ gpulz_status gpulz_compress_split(const void* d_in, size_t n_bytes, int word_siz
         return GPULZ_ERR_INVALID_ARG;
     uint8_t* const ports[3] = {static_cast<uint8_t*>(d_literals), static_cast<uint8_t*>(d_lengths),
                                static_cast<uint8_t*>(d_offsets)};
-    return compress_impl(d_in, n_bytes, word_size, chunk_size, match_level, d_meta, capacity[0],
-                         d_port_bytes, ports, capacity + 1, stream);
+    return compress_impl(d_in, n_bytes, word_size, chunk_size, match_level, 32, d_meta,
+                         capacity[0], d_port_bytes, ports, capacity + 1, stream);
 }
 
 namespace {

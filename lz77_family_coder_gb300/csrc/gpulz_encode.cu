@@ -218,10 +218,165 @@ __device__ __forceinline__ bool chains_live(const uint32_t (&cc)[SEGP], uint32_t
 __device__ __forceinline__ uint32_t expand4(uint32_t bits) { return (bits * 0x00204081u) & 0x01010101u; }
 
 // ---------------------------------------------------------------------------
+// Wider near windows (the window-width study of the match-search section:
+// 48 and 64 elements). Offsets 33..64 get a second set of masks over the same
+// positions: m[p] bit o-1 set iff element (base+p) equals element
+// (base+p-32-o), 1 <= o <= 32, base+p-32-o >= 0, then ANDed with `far_mask`
+// (the offsets 33..window). The longest run over 1..window is the longer of
+// the two passes' runs, the first pass winning ties (its offsets are nearer).
+// ---------------------------------------------------------------------------
+template <int WS>
+__device__ __forceinline__ void load4(const uint8_t* s_el, int i0, uint32_t (&w)[4]) {
+    w[0] = w[1] = w[2] = w[3] = 0u;
+    if (i0 < 0) return;
+    const uint8_t* p = s_el + el_addr<WS>((uint32_t)i0);
+    if (WS == 4) {
+        const uint4 t = *reinterpret_cast<const uint4*>(p);
+        w[0] = t.x; w[1] = t.y; w[2] = t.z; w[3] = t.w;
+    } else if (WS == 2) {
+        const uint2 t = *reinterpret_cast<const uint2*>(p);
+        w[0] = t.x & 0xFFFFu; w[1] = t.x >> 16; w[2] = t.y & 0xFFFFu; w[3] = t.y >> 16;
+    } else {
+        const uint32_t t = *reinterpret_cast<const uint32_t*>(p);
+        w[0] = t & 0xFFu; w[1] = (t >> 8) & 0xFFu; w[2] = (t >> 16) & 0xFFu; w[3] = t >> 24;
+    }
+}
+
+template <int WS, int SEGP>
+__device__ __forceinline__ void near_masks_far(const uint8_t* s_el, uint32_t base, uint32_t far_mask,
+                                               uint32_t (&m)[SEGP]) {
+#pragma unroll
+    for (int h = 0; h < SEGP / 8; ++h) {
+        // elements base+8h-64 .. base+8h-25: the far windows of eight positions
+        const int first = (int)base + 8 * h - 64;  // a multiple of 4
+        uint32_t v[40];
+#pragma unroll
+        for (int q = 0; q < 10; ++q) {
+            uint32_t w[4];
+            load4<WS>(s_el, first + 4 * q, w);
+#pragma unroll
+            for (int r = 0; r < 4; ++r) v[4 * q + r] = w[r];
+        }
+#pragma unroll
+        for (int p = 0; p < 8; ++p) {
+            const uint32_t i = base + (uint32_t)(8 * h + p);
+            const uint32_t x = el_get<WS>(s_el, i);
+            uint32_t mm = 0;
+#pragma unroll
+            for (int o = 1; o <= 32; ++o) mm |= (v[p + 32 - o] == x) ? (1u << (o - 1)) : 0u;
+            if (i < 64u) mm &= i > 32u ? (1u << (i - 32u)) - 1u : 0u;
+            m[8 * h + p] = mm & far_mask;
+        }
+    }
+}
+
+// The AND-chain longest match of E4 for one set of masks: per position of the
+// segment (run length | (offset_base + nearest offset) << 8), two per word.
+// Same steps as the kernel's own E4 (register triangle, lockstep continuation
+// with whole-segment skips); used by the far pass.
+template <int SEGP>
+__device__ __forceinline__ void and_chains(const uint32_t (&m)[SEGP], const uint32_t* s_om,
+                                           const uint32_t* s_sa, uint32_t seg_a, uint32_t E,
+                                           uint32_t off_base, uint32_t (&lw)[SEGP / 2]) {
+    uint32_t cc[SEGP];
+    uint32_t A = 0;
+#pragma unroll
+    for (int p = 0; p < SEGP; ++p) {
+        cc[p] = m[p];
+        A |= (uint32_t)(m[p] != 0u) << p;
+    }
+    uint32_t lb[SEGP / 4];
+#pragma unroll
+    for (int w = 0; w < SEGP / 4; ++w) lb[w] = expand4((A >> (4 * w)) & 15u);
+    uint32_t P = A & (1u << (SEGP - 1));
+#pragma unroll
+    for (int k = 1; k < SEGP; ++k) {
+        const uint32_t act = A & ((1u << (SEGP - k)) - 1u);
+        if (!__any_sync(FULL, act != 0u)) break;
+        uint32_t An = 0;
+#pragma unroll
+        for (int p = 0; p + k < SEGP; ++p) {
+            const uint32_t x = cc[p] & m[p + k];
+            const bool ok = ((act >> p) & 1u) && x != 0u;
+            cc[p] = ok ? x : cc[p];
+            An |= (uint32_t)ok << p;
+        }
+#pragma unroll
+        for (int w = 0; w < SEGP / 4; ++w) lb[w] += expand4((An >> (4 * w)) & 15u);
+        P |= An & (1u << (SEGP - 1 - k));
+        A = An;
+    }
+    if (P) {
+        uint32_t A2 = P;
+        uint32_t st = 0;
+        while (A2 != 0u && seg_a + (uint32_t)SEGP + st < E) {
+            const uint32_t q0 = seg_a + (uint32_t)SEGP + st;
+            if (A2 == (1u << SEGP) - 1u || st >= (uint32_t)SEGP) {
+                const uint32_t j = q0 / (uint32_t)SEGP;
+                const uint32_t p0 = (uint32_t)__ffs(A2) - 1u;
+                const uint32_t room = (uint32_t)kMaxLen - (SEGP - p0 + st);
+                uint32_t take = 0, sa = 0;
+                if (room > 4u * SEGP && q0 + 4u * SEGP <= E) {
+                    sa = s_sa[j] & s_sa[j + 1] & s_sa[j + 2] & s_sa[j + 3];
+                    if (chains_live<SEGP>(cc, A2, sa)) take = 4u * SEGP;
+                }
+                if (!take && room > (uint32_t)SEGP) {
+                    sa = s_sa[j];
+                    if (chains_live<SEGP>(cc, A2, sa)) take = SEGP;
+                }
+                if (take) {
+#pragma unroll
+                    for (int p = 0; p < SEGP; ++p)
+                        if ((A2 >> p) & 1u) cc[p] &= sa;
+#pragma unroll
+                    for (int w = 0; w < SEGP / 4; ++w) lb[w] += take * expand4((A2 >> (4 * w)) & 15u);
+                    st += take;
+                    continue;
+                }
+            }
+            for (int k = 0; k < SEGP && A2 != 0u; ++k, ++st) {
+                const uint32_t om = s_om[om_idx(q0 + (uint32_t)k)];
+                uint32_t An = 0;
+#pragma unroll
+                for (int p = 0; p < SEGP; ++p) {
+                    const uint32_t x = cc[p] & om;
+                    const bool ok = ((A2 >> p) & 1u) && x != 0u;
+                    cc[p] = ok ? x : cc[p];
+                    An |= (uint32_t)ok << p;
+                }
+#pragma unroll
+                for (int w = 0; w < SEGP / 4; ++w) lb[w] += expand4((An >> (4 * w)) & 15u);
+                const int over = (int)(SEGP + st + 1u) - kMaxLen;
+                if (over >= 0) An &= ~((2u << (over < SEGP - 1 ? over : SEGP - 1)) - 1u);
+                A2 = An;
+            }
+        }
+    }
+#pragma unroll
+    for (int p = 0; p < SEGP; p += 2) {
+        const uint32_t l0 = (lb[p >> 2] >> (8 * (p & 3))) & 0xFFu;
+        const uint32_t l1 = (lb[p >> 2] >> (8 * ((p + 1) & 3))) & 0xFFu;
+        const uint32_t lo0 = l0 ? (l0 | ((off_base + (uint32_t)__ffs(cc[p])) << 8)) : 0u;
+        const uint32_t lo1 = l1 ? (l1 | ((off_base + (uint32_t)__ffs(cc[p + 1])) << 8)) : 0u;
+        lw[p >> 1] = lo0 | (lo1 << 16);
+    }
+}
+
+// Per 16-bit half (length | offset << 8): the second value where its length
+// is strictly longer.
+__device__ __forceinline__ uint32_t longer_halves(uint32_t a, uint32_t b) {
+    const uint32_t lo = (b & 0xFFu) > (a & 0xFFu) ? (b & 0xFFFFu) : (a & 0xFFFFu);
+    const uint32_t hi = ((b >> 16) & 0xFFu) > ((a >> 16) & 0xFFu) ? (b >> 16) : (a >> 16);
+    return lo | (hi << 16);
+}
+
+// ---------------------------------------------------------------------------
 // The kernel.
 // ---------------------------------------------------------------------------
-template <int WS, int LEVEL, int SEGP, bool SINGLE>
+template <int WS, int LEVEL, int SEGP, bool SINGLE, int NEARW = 32>
 __global__ void __launch_bounds__(256, 4) encode_kernel(EncodeArgs a) {
+    static_assert(NEARW == 32 || (NEARW == 64 && LEVEL == 0 && !SINGLE),
+                  "wider near windows are a two-pass, level-0 option");
     extern __shared__ __align__(16) uint8_t smem[];
     const int tid = threadIdx.x;
     const int lane = tid & 31;
@@ -424,6 +579,36 @@ __global__ void __launch_bounds__(256, 4) encode_kernel(EncodeArgs a) {
                         dlo[q] = make_uint4(lw[4 * q], lw[4 * q + 1], lw[4 * q + 2], lw[4 * q + 3]);
                 }
                 __syncthreads();
+
+                // ---- E4b (near windows wider than 32): offsets 33..window ----
+                // A second set of masks over the same positions replaces the
+                // first (dead once E4 is done); a far run replaces the near
+                // one only when it is strictly longer.
+                if constexpr (NEARW > 32) {
+                    uint32_t m2[SEGP];
+                    near_masks_far<WS, SEGP>(s_el, seg_a, a.far_mask, m2);
+                    {
+                        uint4* dst = reinterpret_cast<uint4*>(s_om + om_idx(seg_a));
+                        uint32_t sa = m2[0];
+#pragma unroll
+                        for (int q = 0; q < SEGP / 4; ++q) {
+                            dst[q] = make_uint4(m2[4 * q], m2[4 * q + 1], m2[4 * q + 2], m2[4 * q + 3]);
+                            sa &= m2[4 * q] & m2[4 * q + 1] & m2[4 * q + 2] & m2[4 * q + 3];
+                        }
+                        s_sa[tid] = sa;
+                    }
+                    __syncthreads();
+                    uint32_t lw2[SEGP / 2];
+                    and_chains<SEGP>(m2, s_om, s_sa, seg_a, E, 32u, lw2);
+                    uint4* dlo = reinterpret_cast<uint4*>(s_lo + seg_a);
+#pragma unroll
+                    for (int q = 0; q < SEGP / 8; ++q) {
+                        const uint4 o = dlo[q];
+                        dlo[q] = make_uint4(longer_halves(o.x, lw2[4 * q]), longer_halves(o.y, lw2[4 * q + 1]),
+                                            longer_halves(o.z, lw2[4 * q + 2]), longer_halves(o.w, lw2[4 * q + 3]));
+                    }
+                    __syncthreads();
+                }
 
                 // ---- E5: level-1 hashed candidates over 8 sub-blocks ----
                 // The sub-block phases only look the buckets up and insert;
@@ -970,14 +1155,14 @@ cudaError_t shape_for(K kern, int threads, uint32_t smem, LaunchShape& cache) {
     return cudaSuccess;
 }
 
-template <int WS, int LEVEL, bool SINGLE>
+template <int WS, int LEVEL, bool SINGLE, int NEARW = 32>
 cudaError_t launch_t(const EncodeArgs& a, cudaStream_t stream) {
     static thread_local LaunchShape shape16, shape8, shape_copy;
     const EncLayout L = enc_layout(a.chunk_size, a.elems, LEVEL);
     const int threads = 32 * team_warps(a.elems);
     // positions per thread: 8, except 16 for 4096-element chunks
     const bool s16 = a.elems / (uint32_t)threads == 16u;
-    auto kern = s16 ? encode_kernel<WS, LEVEL, 16, SINGLE> : encode_kernel<WS, LEVEL, 8, SINGLE>;
+    auto kern = s16 ? encode_kernel<WS, LEVEL, 16, SINGLE, NEARW> : encode_kernel<WS, LEVEL, 8, SINGLE, NEARW>;
     LaunchShape& shape = s16 ? shape16 : shape8;
     cudaError_t err = shape_for(kern, threads, L.total, shape);
     if (err != cudaSuccess) return err;
@@ -1014,6 +1199,12 @@ cudaError_t launch_t(const EncodeArgs& a, cudaStream_t stream) {
 
 cudaError_t launch_encode(const EncodeArgs& a, int word_size, int match_level, bool single_pass,
                           cudaStream_t stream) {
+    if (a.far_mask != 0u) {  // near window of 33..64 elements: two pass, level 0
+        if (single_pass || match_level != 0) return cudaErrorInvalidValue;
+        if (word_size == 4) return launch_t<4, 0, false, 64>(a, stream);
+        if (word_size == 2) return launch_t<2, 0, false, 64>(a, stream);
+        return launch_t<1, 0, false, 64>(a, stream);
+    }
     if (single_pass) {
         if (word_size == 4) return match_level ? launch_t<4, 1, true>(a, stream) : launch_t<4, 0, true>(a, stream);
         if (word_size == 2) return match_level ? launch_t<2, 1, true>(a, stream) : launch_t<2, 0, true>(a, stream);

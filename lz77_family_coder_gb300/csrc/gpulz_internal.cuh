@@ -322,6 +322,7 @@ struct EncodeArgs {
     uint32_t elems;
     uint32_t n_chunks;
     uint32_t hash_bits;
+    uint32_t far_mask;  // near window 33..64: offsets 33..window as bits 0..window-33; 0 = 32
 };
 
 struct DecodeArgs {

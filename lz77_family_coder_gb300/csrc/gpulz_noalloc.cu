@@ -119,6 +119,7 @@ extern "C" gpulz_status gpulz_compress_noalloc(const void* d_in, size_t n_bytes,
     a.elems = (uint32_t)(chunk_size / word_size);
     a.n_chunks = (uint32_t)chunks;
     a.hash_bits = log2_exact(2u * a.elems);
+    a.far_mask = 0u;
     if (launch_encode(a, word_size, match_level, true, stream) != cudaSuccess)
         return GPULZ_ERR_CUDA;
     noalloc_report<<<1, 32, 0, stream>>>(a.status, a.out_bytes);

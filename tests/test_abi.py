@@ -64,6 +64,11 @@ def test_invalid_arguments_rejected_before_any_launch(g):
     assert g.gpulz_compress(P, 100, 4, 2048, 0, P, 1000, P + 4, 0) == g.GPULZ_ERR_INVALID_ARG
     assert g.gpulz_decompress(0, P, 100, 0) == g.GPULZ_ERR_INVALID_ARG
     assert g.gpulz_decompress(P + 1, P, 100, 0) == g.GPULZ_ERR_INVALID_ARG
+    # near window: 32..64, and above 32 only at level 0
+    for window, lvl in ((31, 0), (65, 0), (0, 0), (48, 1), (64, 1)):
+        assert (g.gpulz_compress_window(P, 100, 4, 2048, lvl, window, P, 1000, P, 0)
+                == g.GPULZ_ERR_INVALID_ARG), (window, lvl)
+    assert g.gpulz_compress_window(P, 100, 3, 2048, 0, 48, P, 1000, P, 0) == g.GPULZ_ERR_INVALID_ARG
 
 
 def test_status_strings(g):
