@@ -22,6 +22,9 @@ def _make_input(spec: str) -> np.ndarray:
         return np.full(int(args[1]), int(args[0], 0), np.uint32).view(np.uint8)
     if kind == "bytes":
         return np.frombuffer(bytes.fromhex(args[0]), np.uint8).copy()
+    if kind == "period_distinct_u32":
+        p, n = int(args[0]), int(args[1])
+        return np.tile(distinct_u32(p), n // p + 1)[:n].view(np.uint8).copy()
     if kind == "zero_then_distinct_u32":
         n = int(args[0])
         return np.concatenate([np.zeros(n, np.uint32), distinct_u32(n)]).view(np.uint8)
@@ -40,6 +43,8 @@ def _layout_stream(layout: str, x: np.ndarray, ws: int, cs: int) -> np.ndarray:
             out += struct.pack("<II", int(args[0], 0), int(args[1], 0))
         elif kind == "raw_copy_of_input":
             out += bytes(x[int(args[0]):int(args[1])])
+        elif kind == "hex":
+            out += bytes.fromhex("".join(args))
         else:
             raise ValueError(part)
     return np.frombuffer(bytes(out), np.uint8).copy()
@@ -68,12 +73,13 @@ def load_all():
         ws = int(meta["word_size"])
         cs = int(meta["chunk_size"])
         levels = [int(v) for v in meta["match_level"].split()]
+        windows = [int(v) for v in meta.get("window", "32").split()]
         x = _make_input(meta["input"])
         assert x.size == int(meta["n_bytes"])
         if hexlines:
             stream = np.frombuffer(bytes.fromhex("".join(hexlines)), np.uint8).copy()
         else:
             stream = _layout_stream(meta["stream_layout"], x, ws, cs)
-        cases.append(dict(name=os.path.basename(path), ws=ws, cs=cs, levels=levels, x=x,
-                          stream=stream))
+        cases.append(dict(name=os.path.basename(path), ws=ws, cs=cs, levels=levels,
+                          windows=windows, x=x, stream=stream))
     return cases

@@ -283,8 +283,9 @@ def test_zero_chunk_sentinel_and_raw(orc):
 @pytest.mark.parametrize("case", goldens.load_all(), ids=lambda c: c["name"])
 def test_golden_streams(orc, case):
     for lvl in case["levels"]:
-        s = orc.compress(case["x"], case["ws"], case["cs"], lvl)
-        assert np.array_equal(s, case["stream"]), lvl
+        for window in case["windows"]:
+            s = orc.compress(case["x"], case["ws"], case["cs"], lvl, window=window)
+            assert np.array_equal(s, case["stream"]), (lvl, window)
     y = orc.decompress(case["stream"], case["x"].size)
     assert np.array_equal(y, case["x"])
     p = streamcheck.check_invariants(case["stream"], case["x"].size)
