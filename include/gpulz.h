@@ -122,8 +122,13 @@ gpulz_status gpulz_compress_window(const void* d_in, size_t n_bytes, int word_si
  *   d_out   device, n_bytes bytes, written only in [d_out, d_out + n_bytes).
  *   n_bytes the original length; a header that disagrees records
  *           GPULZ_ERR_SIZE_MISMATCH and nothing is written.
- * The header is parsed on the device: no host synchronisation, so the call
- * can be captured into a CUDA graph once the stream's scratch exists.
+ * The header is parsed on the device: the call does not synchronise with the
+ * host. CUDA graphs: every call (this one and gpulz_compress) takes fresh
+ * ticket counters and look-back tags from a per-call epoch chosen on the
+ * host, so a graph captured from these calls is correct for its first
+ * launch only; launching it again reuses the captured epoch's spent counters
+ * and leaves chunks undone. Issue the calls directly, or capture a new graph
+ * for each launch.
  */
 gpulz_status gpulz_decompress(const void* d_in, void* d_out, size_t n_bytes, cudaStream_t stream);
 
