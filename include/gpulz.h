@@ -123,12 +123,16 @@ gpulz_status gpulz_compress_window(const void* d_in, size_t n_bytes, int word_si
  *   n_bytes the original length; a header that disagrees records
  *           GPULZ_ERR_SIZE_MISMATCH and nothing is written.
  * The header is parsed on the device: the call does not synchronise with the
- * host. CUDA graphs: every call (this one and gpulz_compress) takes fresh
- * ticket counters and look-back tags from a per-call epoch chosen on the
- * host, so a graph captured from these calls is correct for its first
- * launch only; launching it again reuses the captured epoch's spent counters
- * and leaves chunks undone. Issue the calls directly, or capture a new graph
- * for each launch.
+ * host, and it can be captured into a CUDA graph.
+ *
+ * CUDA graphs (this call, gpulz_decompress_bounded, gpulz_compress,
+ * gpulz_compress_window and the split calls): a call made while its stream
+ * is being captured records, around its kernels, the reset of the ticket
+ * counters and look-back descriptors it uses, so the graph can be launched
+ * any number of times, with new input contents each time (sizes and
+ * pointers are those captured). Capture allocates nothing: the stream needs
+ * its scratch from an earlier direct call of at least the same size on it,
+ * else the call returns GPULZ_ERR_INVALID_ARG during capture.
  */
 gpulz_status gpulz_decompress(const void* d_in, void* d_out, size_t n_bytes, cudaStream_t stream);
 

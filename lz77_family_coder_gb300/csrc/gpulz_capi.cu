@@ -38,9 +38,11 @@ size_t scratch_bytes(uint64_t cap_chunks, uint64_t slot_bytes) {
 }
 
 // Returns the scratch for (current device, stream) with room for `chunks`
-// per-chunk words and `slot_bytes` of slots, and advances its epoch.
+// per-chunk words and `slot_bytes` of slots, and advances its epoch. While the
+// stream is being captured into a graph nothing may be allocated (the graph
+// would own the area): the scratch must already be large enough.
 cudaError_t acquire_scratch(cudaStream_t stream, uint64_t chunks, uint64_t slot_bytes,
-                            Scratch** out, uint32_t* epoch_out) {
+                            bool capturing, Scratch** out, uint32_t* epoch_out) {
     int dev = 0;
     cudaError_t err = cudaGetDevice(&dev);
     if (err != cudaSuccess) return err;
@@ -53,6 +55,7 @@ cudaError_t acquire_scratch(cudaStream_t stream, uint64_t chunks, uint64_t slot_
         g_scratch.push_back(s);
     }
     if (s->base == nullptr || s->cap_chunks < chunks || s->slot_bytes < slot_bytes) {
+        if (capturing) return cudaErrorStreamCaptureUnsupported;
         const uint64_t cap = chunks < 4096 ? 4096 : (chunks > s->cap_chunks ? chunks : s->cap_chunks);
         const uint64_t sb = slot_bytes > s->slot_bytes ? slot_bytes : s->slot_bytes;
         void* p = nullptr;
@@ -88,6 +91,27 @@ cudaError_t acquire_scratch(cudaStream_t stream, uint64_t chunks, uint64_t slot_
     *out = s;
     *epoch_out = s->epoch;
     return cudaSuccess;
+}
+
+// A graph captured from a call launches it again and again with the epoch it
+// took at capture. Each launch starts and ends by putting that epoch's two
+// ticket counters and the tile descriptors back to the clean state (zero: no
+// descriptor carries epoch 0), so every launch, and a direct call that later
+// takes the same epoch, finds them as a fresh epoch.
+cudaError_t clear_epoch_state(const Scratch* s, uint32_t epoch, cudaStream_t stream) {
+    cudaError_t err = cudaMemsetAsync(s->base + kTicketOffset + 2 * sizeof(uint32_t) * epoch, 0,
+                                      2 * sizeof(uint32_t), stream);
+    if (err != cudaSuccess) return err;
+    const ScratchRegions r = scratch_regions(s->cap_chunks, s->slot_bytes);
+    return cudaMemsetAsync(s->base + kStateOffset + r.tdesc, 0, r.offsets - r.tdesc, stream);
+}
+
+// Whether `stream` is being captured into a graph.
+cudaError_t is_capturing(cudaStream_t stream, bool* capturing) {
+    cudaStreamCaptureStatus st = cudaStreamCaptureStatusNone;
+    const cudaError_t err = cudaStreamIsCapturing(stream, &st);
+    *capturing = st != cudaStreamCaptureStatusNone;
+    return err;
 }
 
 Scratch* find_scratch(cudaStream_t stream) {
@@ -135,10 +159,15 @@ gpulz_status compress_impl(const void* d_in, size_t n_bytes, int word_size, int 
     if (!aligned(d_out, 4) || !aligned(d_out_bytes, 8)) return GPULZ_ERR_INVALID_ARG;
     const uint64_t chunks = ((uint64_t)n_bytes + chunk_size - 1) / (uint64_t)chunk_size;
     if (chunks > 0xFFFFFFFFull) return GPULZ_ERR_INVALID_ARG;
+    bool capturing = false;
+    if (is_capturing(stream, &capturing) != cudaSuccess) return GPULZ_ERR_CUDA;
     Scratch* s = nullptr;
     uint32_t epoch = 0;
-    if (acquire_scratch(stream, chunks, chunks * (uint64_t)chunk_size, &s, &epoch) != cudaSuccess)
-        return GPULZ_ERR_CUDA;
+    cudaError_t err = acquire_scratch(stream, chunks, chunks * (uint64_t)chunk_size, capturing,
+                                      &s, &epoch);
+    if (err == cudaErrorStreamCaptureUnsupported) return GPULZ_ERR_INVALID_ARG;
+    if (err != cudaSuccess) return GPULZ_ERR_CUDA;
+    if (capturing && clear_epoch_state(s, epoch, stream) != cudaSuccess) return GPULZ_ERR_CUDA;
     const ScratchRegions r = scratch_regions(s->cap_chunks, s->slot_bytes);
     uint8_t* st = s->base + kStateOffset;
     uint32_t* tickets = reinterpret_cast<uint32_t*>(s->base + kTicketOffset);
@@ -171,6 +200,7 @@ gpulz_status compress_impl(const void* d_in, size_t n_bytes, int word_size, int 
     }
     if (launch_encode(a, word_size, match_level, false, stream) != cudaSuccess)
         return GPULZ_ERR_CUDA;
+    if (capturing && clear_epoch_state(s, epoch, stream) != cudaSuccess) return GPULZ_ERR_CUDA;
     return GPULZ_OK;
 }
 }  // namespace
@@ -219,9 +249,14 @@ gpulz_status decompress_impl(const void* d_in, size_t in_bytes, void* d_out, siz
     if (d_in == nullptr || (n_bytes > 0 && d_out == nullptr)) return GPULZ_ERR_INVALID_ARG;
     if (!aligned(d_in, 4)) return GPULZ_ERR_INVALID_ARG;
     const uint64_t max_chunks = ((uint64_t)n_bytes + 1023u) / 1024u;
+    bool capturing = false;
+    if (is_capturing(stream, &capturing) != cudaSuccess) return GPULZ_ERR_CUDA;
     Scratch* s = nullptr;
     uint32_t epoch = 0;
-    if (acquire_scratch(stream, max_chunks, 0, &s, &epoch) != cudaSuccess) return GPULZ_ERR_CUDA;
+    const cudaError_t err = acquire_scratch(stream, max_chunks, 0, capturing, &s, &epoch);
+    if (err == cudaErrorStreamCaptureUnsupported) return GPULZ_ERR_INVALID_ARG;
+    if (err != cudaSuccess) return GPULZ_ERR_CUDA;
+    if (capturing && clear_epoch_state(s, epoch, stream) != cudaSuccess) return GPULZ_ERR_CUDA;
     const ScratchRegions r = scratch_regions(s->cap_chunks, s->slot_bytes);
     uint8_t* st = s->base + kStateOffset;
     uint32_t* tickets = reinterpret_cast<uint32_t*>(s->base + kTicketOffset);
@@ -243,6 +278,7 @@ gpulz_status decompress_impl(const void* d_in, size_t in_bytes, void* d_out, siz
         a.port_len[k] = ports ? port_len[k] : 0;
     }
     if (launch_decode(a, stream) != cudaSuccess) return GPULZ_ERR_CUDA;
+    if (capturing && clear_epoch_state(s, epoch, stream) != cudaSuccess) return GPULZ_ERR_CUDA;
     return GPULZ_OK;
 }
 }  // namespace
