@@ -18,12 +18,14 @@ def to_dev(x: np.ndarray, pad: int = 0):
     return t
 
 
-def gpu_compress(x: np.ndarray, ws: int, cs: int, lvl: int, stream=None) -> np.ndarray:
+def gpu_compress(x: np.ndarray, ws: int, cs: int, lvl: int, stream=None,
+                 window: int = 32) -> np.ndarray:
     """Compress host bytes on the GPU; returns the stream bytes (host)."""
     import torch
     g = lib()
     d_in = to_dev(x)
-    out, nbytes = g.compress(d_in[:x.size] if x.size else d_in, ws, cs, lvl, stream=stream)
+    out, nbytes = g.compress(d_in[:x.size] if x.size else d_in, ws, cs, lvl, stream=stream,
+                             window=window)
     st = g.gpulz_device_status(stream)
     assert st == g.GPULZ_OK, g.gpulz_status_string(st)
     n = int(nbytes.item())

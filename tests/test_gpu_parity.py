@@ -100,8 +100,9 @@ def test_plane_sample_all_geometries(orc, ws, cs, lvl):
 @pytest.mark.parametrize("case", goldens.load_all(), ids=lambda c: c["name"])
 def test_golden_streams_on_gpu(case):
     for lvl in case["levels"]:
-        s = gpu_compress(case["x"], case["ws"], case["cs"], lvl)
-        assert np.array_equal(s, case["stream"])
+        for window in case["windows"]:
+            s = gpu_compress(case["x"], case["ws"], case["cs"], lvl, window=window)
+            assert np.array_equal(s, case["stream"]), (lvl, window)
     assert np.array_equal(gpu_decompress(case["stream"], case["x"].size), case["x"])
 
 
