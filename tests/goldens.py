@@ -28,6 +28,26 @@ def _make_input(spec: str) -> np.ndarray:
     if kind == "zero_then_distinct_u32":
         n = int(args[0])
         return np.concatenate([np.zeros(n, np.uint32), distinct_u32(n)]).view(np.uint8)
+    if kind == "distinct_u32_with":
+        # n distinct words, then edits in order:
+        #   copy:dst:src:len  w[dst + k] = w[src + k] for k < len
+        #   set:i:value       w[i] = value
+        #   pairs:start:count w[start + 2j + 1] = w[start + 2j] for j < count
+        w = distinct_u32(int(args[0]))
+        for op in args[1:]:
+            name, *v = op.split(":")
+            v = [int(t, 0) for t in v]
+            if name == "copy":
+                for k in range(v[2]):
+                    w[v[0] + k] = w[v[1] + k]
+            elif name == "set":
+                w[v[0]] = v[1]
+            elif name == "pairs":
+                for j in range(v[1]):
+                    w[v[0] + 2 * j + 1] = w[v[0] + 2 * j]
+            else:
+                raise ValueError(op)
+        return w.view(np.uint8).copy()
     raise ValueError(spec)
 
 

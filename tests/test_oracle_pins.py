@@ -11,11 +11,15 @@ cap, a flipped flag polarity, a wrong raw threshold) fails at least one:
   chunk at level 1 (only the hashed table can see it, and only from earlier
   sub-blocks, keeping the most recent position), zero chunk, incompressible
   chunk;
-* hand-derived golden streams (tests/golden/);
+* hand-derived golden streams (tests/golden/), among them a level-1 chunk
+  whose bytes depend on a bucket collision (hash, table size, max rule), the
+  word-size-2 minimum match length from both sides and the raw threshold from
+  both sides; the bucket hash worked out by hand for four table sizes;
 * structural invariants and an independent replay decoder on every stream;
 * round trip through the oracle's own decoder, both levels, all geometries.
 """
 import itertools
+import os
 
 import numpy as np
 import pytest
@@ -265,6 +269,35 @@ def test_level1_table_definition_tiny(orc):
                         if k > el or (k == el and k > 0 and d < eo):
                             el, eo = k, d
                 assert (L1[i], O1[i]) == (el, eo), (E, alphabet, i)
+
+
+def _hash_table_rows():
+    rows = []
+    with open(os.path.join(goldens.GOLDEN_DIR, "level1_hash_values.tab")) as f:
+        for line in f:
+            if line.strip() and not line.startswith("#"):
+                rows.append([int(v, 0) for v in line.split()])
+    return rows
+
+
+def test_level1_hash_values(orc):
+    """The bucket of a two-word key and the table size against values worked
+    out by hand from the documented formula (tests/golden/level1_hash_values.tab):
+    a slip in either multiplier, the xor, the shift or log2(2E) changes a row."""
+    rows = _hash_table_rows()
+    assert len(rows) >= 20
+    for E, B, k0, k1, p0, p1, x, h in rows:
+        # the row's own arithmetic (guards the table against a typo)
+        assert p0 ^ p1 == x and x >> (32 - B) == h
+        assert orc.hash_bits(E) == B, (E, B)
+        assert orc.hash2(k0, k1, B) == h, (E, k0, k1)
+
+
+def test_min_match_len_each_word_size(orc):
+    """A token (2 bytes) is taken only when its literals would take more: the
+    shortest match is 3, 2 and 1 elements for word sizes 1, 2 and 4 (the
+    abcab, lmin_ws2 and constant goldens show each one in a stream)."""
+    assert [orc.min_match_len(ws) for ws in (1, 2, 4)] == [3, 2, 1]
 
 
 def _one_chunk_stream(orc, x, ws, cs, lvl):
