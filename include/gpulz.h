@@ -37,7 +37,10 @@
  * is placed (so about n_bytes of scratch for an n_bytes input). The first
  * call on a stream, or a call needing more room than any earlier call on it,
  * allocates that scratch stream-ordered (cudaMallocAsync); later calls
- * allocate nothing. gpulz_compress_noalloc never allocates.
+ * allocate nothing. The scratch lives until gpulz_release_scratch(stream) is
+ * called (or the process exits): a caller that makes short-lived streams
+ * releases each one's scratch before destroying the stream.
+ * gpulz_compress_noalloc never allocates.
  *
  * Errors: argument errors a host can check are returned synchronously and
  * nothing is launched. Conditions found on the device (corrupt stream, size
@@ -155,6 +158,20 @@ gpulz_status gpulz_stream_info(const void* h_header, size_t h_len, size_t* orig_
 gpulz_status gpulz_device_status(cudaStream_t stream);
 
 /*
+ * gpulz_release_scratch -- give back the scratch the library holds for
+ * `stream` on the current device (no counterpart in the paper: the lifetime
+ * of this library's own scratch).
+ *
+ * The memory is freed stream-ordered (cudaFreeAsync on `stream`), so work
+ * already enqueued on the stream finishes first; the stream must still be
+ * valid. A status the device recorded on this stream and not yet read by
+ * gpulz_device_status() is dropped with it. The next call on the stream
+ * allocates afresh. Returns GPULZ_OK if the stream holds no scratch, and
+ * GPULZ_ERR_INVALID_ARG (nothing freed) while the stream is being captured.
+ */
+gpulz_status gpulz_release_scratch(cudaStream_t stream);
+
+/*
  * gpulz_compress_noalloc -- gpulz_compress for callers that cannot allocate.
  * (No counterpart in the paper: the GPULZ pages have no such entry point.)
  *
@@ -173,9 +190,10 @@ gpulz_status gpulz_device_status(cudaStream_t stream);
  * GPULZ_ERR_INVALID_ARG and launch nothing.
  * Set-up: the first call on a device looks up the array's device address with
  * that device current; make that first call before any stream capture.
- * Sharing: all calls on a device share the one array and each call clears it
- * on its stream first, so calls that overlap on the GPU (other streams, other
- * host threads) race and must not be issued. A device-side wait that gives up
+ * Sharing: all calls on a device share the one array, which keeps the last
+ * call's contents; each call first clears, on its stream, the part it uses
+ * (status word, ticket, one look-back entry per chunk). Calls that overlap on
+ * the GPU (other streams, other host threads) race and must not be issued. A device-side wait that gives up
  * sets *d_out_bytes to SIZE_MAX; capacity overflow shows as
  * *d_out_bytes > capacity. gpulz_device_status() does not see this path.
  */

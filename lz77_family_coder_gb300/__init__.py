@@ -22,7 +22,7 @@ __all__ = [
     "gpulz_decompress_bounded", "gpulz_compress_bound", "gpulz_stream_info",
     "gpulz_device_status", "gpulz_set_kernel_events", "gpulz_status_string", "compress",
     "decompress", "gpulz_split_bounds", "gpulz_compress_split", "gpulz_decompress_split",
-    "compress_split", "decompress_split",
+    "compress_split", "decompress_split", "gpulz_release_scratch", "gpulz_test_lookback",
 ]
 
 GPULZ_OK = 0
@@ -91,6 +91,11 @@ def load():
     lib.gpulz_set_kernel_events.restype = i32
     lib.gpulz_status_string.argtypes = [i32]
     lib.gpulz_status_string.restype = ctypes.c_char_p
+    lib.gpulz_release_scratch.argtypes = [vp]
+    lib.gpulz_release_scratch.restype = i32
+    lib.gpulz_test_lookback.argtypes = [vp, ctypes.c_uint32, ctypes.c_uint64, ctypes.c_uint32,
+                                        ctypes.c_uint64, vp, vp]
+    lib.gpulz_test_lookback.restype = i32
     _lib = lib
     return lib
 
@@ -205,6 +210,17 @@ def gpulz_set_kernel_events(start, stop) -> int:
 
 def gpulz_status_string(status: int) -> str:
     return load().gpulz_status_string(status).decode()
+
+
+def gpulz_release_scratch(stream=None) -> int:
+    return load().gpulz_release_scratch(_stream(stream))
+
+
+def gpulz_test_lookback(d_desc, idx, value, epoch, limit_ns, d_prefix, stream=None) -> int:
+    """Test hook (include/gpulz_testing.h): the library's bounded look-back on a
+    caller-made descriptor array."""
+    return load().gpulz_test_lookback(_ptr(d_desc), idx, value, epoch, limit_ns, _ptr(d_prefix),
+                                      _stream(stream))
 
 
 # ---- conveniences (torch allocates, the library computes) ----

@@ -18,7 +18,8 @@ CSRC = os.path.join(HERE, "csrc")
 LIBDIR = os.path.join(HERE, "_lib")
 LIB = os.path.join(LIBDIR, "libgpulz.so")
 SOURCES = ["gpulz_encode.cu", "gpulz_decode.cu", "gpulz_capi.cu", "gpulz_noalloc.cu"]
-HEADERS = ["gpulz_internal.cuh", os.path.join("..", "..", "include", "gpulz.h")]
+HEADERS = ["gpulz_internal.cuh", os.path.join("..", "..", "include", "gpulz.h"),
+           os.path.join("..", "..", "include", "gpulz_testing.h")]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-Wall",
               "-I" + os.path.join(ROOT, "include")]

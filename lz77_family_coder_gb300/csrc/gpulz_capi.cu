@@ -9,6 +9,7 @@
 #include <vector>
 
 #include "../../include/gpulz.h"
+#include "../../include/gpulz_testing.h"
 #include "gpulz_internal.cuh"
 
 namespace {
@@ -112,6 +113,36 @@ cudaError_t is_capturing(cudaStream_t stream, bool* capturing) {
     const cudaError_t err = cudaStreamIsCapturing(stream, &st);
     *capturing = st != cudaStreamCaptureStatusNone;
     return err;
+}
+
+// Removes and returns the scratch entry of (current device, stream), or null.
+Scratch* take_scratch(cudaStream_t stream) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return nullptr;
+    std::lock_guard<std::mutex> lock(g_mu);
+    for (size_t k = 0; k < g_scratch.size(); ++k) {
+        Scratch* t = g_scratch[k];
+        if (t->device == dev && t->stream == stream) {
+            g_scratch.erase(g_scratch.begin() + (long)k);
+            return t;
+        }
+    }
+    return nullptr;
+}
+
+// Test hook: one warp runs the library's look-back over a caller-made
+// descriptor array with the given wait limit; a wait that gives up records
+// the timeout in the stream's status word, as the coder's kernels do.
+__global__ void lookback_probe(uint64_t* desc, uint32_t idx, uint64_t value, uint32_t epoch,
+                               uint64_t limit_ns, unsigned long long* prefix_out,
+                               uint32_t* status) {
+    const int lane = threadIdx.x & 31;
+    bool to = false;
+    const uint64_t prefix = lookback(desc, idx, value, epoch, lane, &to, limit_ns);
+    if (lane == 0) {
+        *prefix_out = prefix;
+        if (to) atomicOr(status, kStatTimeout);
+    }
 }
 
 Scratch* find_scratch(cudaStream_t stream) {
@@ -343,6 +374,40 @@ gpulz_status gpulz_device_status(cudaStream_t stream) {
     if (bits & kStatTimeout) return GPULZ_ERR_TIMEOUT;
     if (bits & kStatCapacity) return GPULZ_ERR_CAPACITY;
     return GPULZ_OK;
+}
+
+gpulz_status gpulz_release_scratch(cudaStream_t stream) {
+    if (find_scratch(stream) == nullptr) {
+        // nothing held (an entry whose allocation failed holds no memory)
+        delete take_scratch(stream);
+        return GPULZ_OK;
+    }
+    bool capturing = false;
+    if (is_capturing(stream, &capturing) != cudaSuccess) return GPULZ_ERR_CUDA;
+    if (capturing) return GPULZ_ERR_INVALID_ARG;
+    Scratch* s = take_scratch(stream);
+    if (s == nullptr) return GPULZ_OK;
+    const cudaError_t err = s->base ? cudaFreeAsync(s->base, stream) : cudaSuccess;
+    delete s;
+    return err == cudaSuccess ? GPULZ_OK : GPULZ_ERR_CUDA;
+}
+
+gpulz_status gpulz_test_lookback(uint64_t* d_desc, uint32_t idx, uint64_t value, uint32_t epoch,
+                                 uint64_t limit_ns, size_t* d_prefix, cudaStream_t stream) {
+    if (d_desc == nullptr || d_prefix == nullptr || epoch == 0 || epoch >= kEpochs ||
+        limit_ns > kWaitLimitNs || !aligned(d_desc, 8) || !aligned(d_prefix, 8))
+        return GPULZ_ERR_INVALID_ARG;
+    bool capturing = false;
+    if (is_capturing(stream, &capturing) != cudaSuccess) return GPULZ_ERR_CUDA;
+    Scratch* s = nullptr;
+    uint32_t scratch_epoch = 0;
+    const cudaError_t err = acquire_scratch(stream, 0, 0, capturing, &s, &scratch_epoch);
+    if (err == cudaErrorStreamCaptureUnsupported) return GPULZ_ERR_INVALID_ARG;
+    if (err != cudaSuccess) return GPULZ_ERR_CUDA;
+    lookback_probe<<<1, 32, 0, stream>>>(d_desc, idx, value, epoch, limit_ns,
+                                         reinterpret_cast<unsigned long long*>(d_prefix),
+                                         reinterpret_cast<uint32_t*>(s->base));
+    return cudaGetLastError() == cudaSuccess ? GPULZ_OK : GPULZ_ERR_CUDA;
 }
 
 gpulz_status gpulz_set_kernel_events(cudaEvent_t start, cudaEvent_t stop) {

@@ -481,9 +481,10 @@ __global__ void __launch_bounds__(kDecWarps * 32) decode_kernel(DecodeArgs a) {
 }  // namespace
 
 cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t stream) {
-    static int configured_dev = -1;
-    static int grid_cache = 0;
-    static int sms_cache = 0;
+    // launch shape of the device last used by this host thread
+    static thread_local int configured_dev = -1;
+    static thread_local int grid_cache = 0;
+    static thread_local int sms_cache = 0;
     int dev = 0;
     cudaError_t err = cudaGetDevice(&dev);
     if (err != cudaSuccess) return err;

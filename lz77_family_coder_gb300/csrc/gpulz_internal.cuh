@@ -175,10 +175,10 @@ __device__ __forceinline__ LBStep lb_step(const uint64_t* arr, int64_t top, uint
 }
 
 // Lane 0 polls one descriptor, backing off, until it carries this call's
-// epoch. Returns false if the wait gave up after kWaitLimitNs (measured from
-// *t0, set on the first wait).
+// epoch. Returns false if the wait gave up after limit_ns (measured from *t0,
+// set on the first wait).
 __device__ __forceinline__ bool wait_published(const uint64_t* arr, int64_t idx, uint32_t epoch,
-                                               int lane, uint64_t* t0) {
+                                               int lane, uint64_t* t0, uint64_t limit_ns) {
     bool ok = true;
     if (lane == 0) {
         uint32_t ns = 32;
@@ -187,7 +187,7 @@ __device__ __forceinline__ bool wait_published(const uint64_t* arr, int64_t idx,
             if (desc_epoch(d) == epoch && desc_kind(d) != 0) break;
             const uint64_t now = globaltimer_ns();
             if (*t0 == 0) *t0 = now;
-            if (now - *t0 > kWaitLimitNs) {
+            if (now - *t0 > limit_ns) {
                 ok = false;
                 break;
             }
@@ -201,9 +201,13 @@ __device__ __forceinline__ bool wait_published(const uint64_t* arr, int64_t idx,
 // Exclusive prefix of `value` over entries [0, idx) of arr (one warp). The
 // caller has published arr[idx] (aggregate). Publishes arr[idx]'s inclusive
 // prefix. Every wait is on entries with smaller tickets, which publish their
-// aggregates without waiting.
+// aggregates without waiting. A wait that gives up (limit_ns) sets
+// *timed_out; arr[idx] is then still published, with the partial sum, so that
+// later entries do not wait as well (the caller records the timeout, which
+// marks the whole result invalid).
 __device__ __forceinline__ uint64_t lookback(uint64_t* arr, uint32_t idx, uint64_t value,
-                                             uint32_t epoch, int lane, bool* timed_out) {
+                                             uint32_t epoch, int lane, bool* timed_out,
+                                             uint64_t limit_ns = kWaitLimitNs) {
     *timed_out = false;
     uint64_t prefix = 0;
     int64_t top = (int64_t)idx - 1;
@@ -211,7 +215,7 @@ __device__ __forceinline__ uint64_t lookback(uint64_t* arr, uint32_t idx, uint64
     while (top >= 0) {
         const LBStep r = lb_step(arr, top, kLBWidth, epoch, lane);
         if (r.wait) {
-            if (!wait_published(arr, top - (int64_t)r.first_bad, epoch, lane, &t0)) {
+            if (!wait_published(arr, top - (int64_t)r.first_bad, epoch, lane, &t0, limit_ns)) {
                 *timed_out = true;
                 break;
             }

@@ -36,9 +36,11 @@ uint32_t g_epoch[kMaxDevices] = {};  // last epoch used on each device
 
 // Device address of g_noalloc_scratch on the current device, looked up once
 // per device with that device current, and the next epoch for this call.
-// Look-back entries carry the epoch of the call that wrote them, so only the
-// status word and the ticket have to be cleared per call; when the 16-bit
-// epoch wraps, the whole array is cleared once (*clear_all).
+// Look-back entries carry the epoch of the call that wrote them, and every
+// call also clears, on its stream, the status word, the ticket and the entries
+// of the chunks it codes, so no entry left by an earlier call (whatever its
+// epoch) can be taken for one of this call's; on first use the whole array is
+// cleared (*clear_all).
 cudaError_t scratch_address(uint8_t** out, uint32_t* epoch, bool* clear_all) {
     int dev = 0;
     cudaError_t err = cudaGetDevice(&dev);
@@ -55,10 +57,7 @@ cudaError_t scratch_address(uint8_t** out, uint32_t* epoch, bool* clear_all) {
         g_epoch[dev] = 0;
     }
     g_epoch[dev] += 1;
-    if (g_epoch[dev] >= kEpochs) {
-        g_epoch[dev] = 1;
-        *clear_all = true;
-    }
+    if (g_epoch[dev] >= kEpochs) g_epoch[dev] = 1;
     *out = g_scratch_dev[dev];
     *epoch = g_epoch[dev];
     return cudaSuccess;
@@ -88,10 +87,11 @@ extern "C" gpulz_status gpulz_compress_noalloc(const void* d_in, size_t n_bytes,
     uint32_t epoch = 0;
     bool clear_all = false;
     if (scratch_address(&base, &epoch, &clear_all) != cudaSuccess) return GPULZ_ERR_CUDA;
-    // The array keeps the previous call's contents: clear the status word and
-    // the ticket (all of it on first use and when the epoch wraps), in stream
-    // order.
-    if (cudaMemsetAsync(base, 0, clear_all ? kNoAllocBytes : kNoAllocHead, stream) != cudaSuccess)
+    // The array keeps the previous call's contents: clear the status word, the
+    // ticket and this call's look-back entries (all of it on first use), in
+    // stream order.
+    const size_t used = kNoAllocHead + sizeof(uint64_t) * (size_t)chunks;
+    if (cudaMemsetAsync(base, 0, clear_all ? kNoAllocBytes : used, stream) != cudaSuccess)
         return GPULZ_ERR_CUDA;
     EncodeArgs a;
     a.in = static_cast<const uint8_t*>(d_in);

@@ -19,14 +19,20 @@ def g():
 
 
 def declared_functions():
-    text = open(os.path.join(ROOT, "include", "gpulz.h")).read()
-    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
-    return sorted(set(re.findall(r"\b(gpulz_\w+)\s*\(", text)))
+    names = set()
+    for h in sorted(os.listdir(os.path.join(ROOT, "include"))):
+        if not h.endswith(".h"):
+            continue
+        text = open(os.path.join(ROOT, "include", h)).read()
+        text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+        names |= set(re.findall(r"\b(gpulz_\w+)\s*\(", text))
+    return sorted(names)
 
 
 def test_exports_every_declared_symbol(g):
     names = declared_functions()
-    assert {"gpulz_compress", "gpulz_decompress"} <= set(names)
+    assert {"gpulz_compress", "gpulz_decompress", "gpulz_release_scratch",
+            "gpulz_test_lookback"} <= set(names)
     lib = g.load()
     for n in names:
         assert hasattr(lib, n), n
@@ -81,3 +87,17 @@ def test_kernel_events_hook_arguments(g):
     assert g.gpulz_set_kernel_events(1 << 20, None) == g.GPULZ_ERR_INVALID_ARG
     assert g.gpulz_set_kernel_events(None, 1 << 20) == g.GPULZ_ERR_INVALID_ARG
     assert g.gpulz_set_kernel_events(None, None) == g.GPULZ_OK
+
+
+def test_release_and_test_hook_arguments(g):
+    """Releasing a stream that holds no scratch is a no-op; the look-back test
+    hook refuses bad arguments before touching the GPU."""
+    P = 1 << 20
+    assert g.gpulz_release_scratch(0) == g.GPULZ_OK
+    assert g.gpulz_test_lookback(0, 3, 1, 5, 1000, P, 0) == g.GPULZ_ERR_INVALID_ARG
+    assert g.gpulz_test_lookback(P, 3, 1, 5, 1000, 0, 0) == g.GPULZ_ERR_INVALID_ARG
+    assert g.gpulz_test_lookback(P, 3, 1, 0, 1000, P, 0) == g.GPULZ_ERR_INVALID_ARG
+    assert g.gpulz_test_lookback(P, 3, 1, 65536, 1000, P, 0) == g.GPULZ_ERR_INVALID_ARG
+    assert g.gpulz_test_lookback(P + 4, 3, 1, 5, 1000, P, 0) == g.GPULZ_ERR_INVALID_ARG
+    assert (g.gpulz_test_lookback(P, 3, 1, 5, 200 * 1000 * 1000 + 1, P, 0)
+            == g.GPULZ_ERR_INVALID_ARG)

@@ -196,3 +196,82 @@ def test_kernel_events_hook_brackets_the_main_kernels(orc):
     assert g.gpulz_compress(d_in, x.size, 4, 2048, 0, out, cap, nb) == g.GPULZ_OK
     torch.cuda.synchronize()
     assert ev[1].elapsed_time(ev[2]) == stamp
+
+
+# ---------------------------------------------------------------------------
+# bounded device waits: a look-back whose predecessor never publishes gives up
+# after its limit, records the timeout and returns (the context stays usable)
+# ---------------------------------------------------------------------------
+def _desc(epoch, kind, value):
+    return (epoch << 48) | (kind << 46) | value
+
+
+def test_bounded_lookback_wait_times_out(orc):
+    import time
+    import torch
+    g = lib()
+    n, idx, ep = 100, 99, 7
+    arr = np.array([_desc(ep, 2 if k == 0 else 1, k + 1) for k in range(n)], np.uint64)
+    pre = torch.full((1,), -1, dtype=torch.int64, device="cuda")
+    assert g.gpulz_device_status() == g.GPULZ_OK
+    # control: every predecessor published -> exact prefix, no timeout
+    d = torch.from_numpy(arr.view(np.int64).copy()).cuda()
+    assert g.gpulz_test_lookback(d, idx, 5, ep, 20_000_000, pre) == g.GPULZ_OK
+    assert g.gpulz_device_status() == g.GPULZ_OK
+    total = sum(range(1, idx + 1))
+    assert int(pre.item()) == total
+    after = d.cpu().numpy().view(np.uint64)
+    assert np.array_equal(after[:idx], arr[:idx])
+    assert int(after[idx]) == _desc(ep, 2, total + 5)
+    # entry 37 carries another call's epoch: it is never published for this one
+    bad = arr.copy()
+    bad[37] = _desc(ep - 1, 1, 38)
+    d = torch.from_numpy(bad.view(np.int64).copy()).cuda()
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    assert g.gpulz_test_lookback(d, idx, 5, ep, 20_000_000, pre) == g.GPULZ_OK
+    st = g.gpulz_device_status()
+    dt = time.perf_counter() - t0
+    assert st == g.GPULZ_ERR_TIMEOUT
+    assert 0.02 <= dt < 5.0, dt
+    after = d.cpu().numpy().view(np.uint64)
+    assert np.array_equal(after[:idx], bad[:idx])      # nothing below idx was written
+    assert (int(after[idx]) >> 46) == (ep << 2) | 2     # idx published (inclusive, partial)
+    assert g.gpulz_device_status() == g.GPULZ_OK        # the status was read and cleared
+    # the context is still usable
+    x = _workload(200000)
+    assert np.array_equal(gpu_compress(x, 4, 2048, 1), orc.compress(x, 4, 2048, 1))
+
+
+# ---------------------------------------------------------------------------
+# scratch lifetime: per-stream scratch is given back by gpulz_release_scratch
+# ---------------------------------------------------------------------------
+def test_release_scratch_returns_memory():
+    import torch
+    g = lib()
+    n, cs = 512 << 20, 4096
+    d_in = torch.zeros(n, dtype=torch.uint8, device="cuda")
+    streams = [torch.cuda.Stream() for _ in range(8)]
+    outs = [torch.empty(2 << 20, dtype=torch.uint8, device="cuda") for _ in streams]
+    nbs = [torch.zeros(1, dtype=torch.int64, device="cuda") for _ in streams]
+    torch.cuda.synchronize()
+    free0 = torch.cuda.mem_get_info()[0]
+    for s, o, nb in zip(streams, outs, nbs):
+        assert g.gpulz_compress(d_in, n, 4, cs, 0, o, o.numel(), nb, s) == g.GPULZ_OK
+    torch.cuda.synchronize()
+    held = free0 - torch.cuda.mem_get_info()[0]
+    assert held >= 8 * n * 0.9, held                      # a slot area per stream
+    for s, nb in zip(streams, nbs):
+        assert g.gpulz_device_status(s) == g.GPULZ_OK
+        assert int(nb.item()) == 32 + 8 * (n // cs)       # all-zero chunks
+        assert g.gpulz_release_scratch(s) == g.GPULZ_OK
+        assert g.gpulz_release_scratch(s) == g.GPULZ_OK   # nothing left: a no-op
+    torch.cuda.synchronize()
+    left = free0 - torch.cuda.mem_get_info()[0]
+    assert left < (64 << 20), left
+    # a released stream allocates afresh on its next call
+    s, o, nb = streams[0], outs[0], nbs[0]
+    assert g.gpulz_compress(d_in[:1 << 20], 1 << 20, 4, cs, 1, o, o.numel(), nb, s) == g.GPULZ_OK
+    assert g.gpulz_device_status(s) == g.GPULZ_OK
+    assert int(nb.item()) == 32 + 8 * ((1 << 20) // cs)
+    assert g.gpulz_release_scratch(s) == g.GPULZ_OK
