@@ -27,10 +27,16 @@ Everything is deterministic in the seed (numpy PCG64).
 """
 from __future__ import annotations
 
+import concurrent.futures
 import dataclasses
 import math
+import os
 
 import numpy as np
+
+
+def _workers() -> int:
+    return max(1, min(16, os.cpu_count() or 1))
 
 
 @dataclasses.dataclass(frozen=True)
@@ -129,16 +135,28 @@ def generate_field(cfg: Config, seed: int | None = None) -> np.ndarray:
         noisy = clean + rng.normal(0.0, 1e-3 * rng_f, size=clean.shape)
         return noisy.astype(np.float32)
     nz, ny, nx = cfg.shape
-    lo, hi = math.inf, -math.inf
-    for z in range(nz):
-        plane = _plane_sum(terms, ny, nx, float(z))
-        lo = min(lo, float(plane.min()))
-        hi = max(hi, float(plane.max()))
-    sigma = 1e-3 * (hi - lo)
-    out = np.empty(cfg.shape, np.float32)
-    for z in range(nz):
-        plane = _plane_sum(terms, ny, nx, float(z))
-        out[z] = (plane + rng.normal(0.0, sigma, size=plane.shape)).astype(np.float32)
+    workers = _workers()
+
+    def plane_at(z):
+        return _plane_sum(terms, ny, nx, float(z))
+
+    def extent(z):
+        plane = plane_at(z)
+        return float(plane.min()), float(plane.max())
+
+    # the planes are independent (computed on host threads, in any order); the
+    # noise is drawn in z order from the one generator, so the field does not
+    # depend on the number of threads
+    with concurrent.futures.ThreadPoolExecutor(workers) as ex:
+        ext = list(ex.map(extent, range(nz)))
+        lo = min(e[0] for e in ext)
+        hi = max(e[1] for e in ext)
+        sigma = 1e-3 * (hi - lo)
+        out = np.empty(cfg.shape, np.float32)
+        for z0 in range(0, nz, workers):
+            zs = range(z0, min(nz, z0 + workers))
+            for z, plane in zip(zs, ex.map(plane_at, zs)):
+                out[z] = (plane + rng.normal(0.0, sigma, size=plane.shape)).astype(np.float32)
     return out
 
 
@@ -171,14 +189,19 @@ def lorenzo_codes(field: np.ndarray, cfg: Config) -> np.ndarray:
         return np.clip(delta + R, 0, 2 * R - 1).astype(dt)
     out = np.empty(field.shape, dt)
     nz = field.shape[0]
-    q_prev = None
-    for z in range(nz):
-        q = _round_half_away(field[z].astype(np.float64) / (2.0 * eb))
-        d2 = _lorenzo_2d(q)
-        if cfg.lorenzo == "3d" and q_prev is not None:
-            d2 = d2 - _lorenzo_2d(q_prev)
+
+    def quant(z):
+        return _round_half_away(field[z].astype(np.float64) / (2.0 * eb))
+
+    def slice_codes(z):
+        # 3D: the 2D delta of slice z minus that of slice z - 1 (zero outside)
+        d2 = _lorenzo_2d(quant(z))
+        if cfg.lorenzo == "3d" and z > 0:
+            d2 = d2 - _lorenzo_2d(quant(z - 1))
         out[z] = np.clip(d2 + R, 0, 2 * R - 1).astype(dt)
-        q_prev = q
+
+    with concurrent.futures.ThreadPoolExecutor(_workers()) as ex:
+        list(ex.map(slice_codes, range(nz)))
     return out
 
 
