@@ -1,13 +1,20 @@
 #!/usr/bin/env python3
-"""Benchmark of the GPULZ coder on GB300: one step = encode + decode of one
-1800x3600 uint32 Lorenzo-code field (25.92 MB, chunk_size 2048, word_size 4,
-match level 0), inputs resident in HBM.
+"""Benchmark of the GPULZ coder on GB300: one step = encode + decode of the
+512x512x512 uint32 Lorenzo-code volume (536.9 MB, chunk_size 4096, word_size 4,
+match level 1), the largest of the five workloads, inputs resident in HBM.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                    [--config ID] [--no-per-config] [--window W] [--split]
 
-Prints ONE JSON line (rank 0). With N > 1 (torchrun), every rank codes its own
-copy of the workload (weak scaling, no data-path collective); the timed region
-is bracketed by a barrier + synchronize and the max over ranks is taken.
+Prints ONE JSON line (rank 0). `value` is the round-trip throughput (input
+bytes / (encode time + decode time)); the line also carries encode and decode
+GB/s, the ratio, the HBM roofline fraction of the encode kernel (headline) and
+of the decode kernel, and a `per_config` table in which each of the five
+workloads is timed the same way and checked against the oracle in this run.
+L2 is flushed (a 256 MB write) before every timed encode and every timed
+decode. With N > 1 (torchrun), every rank codes its own copy of the workload
+(weak scaling, no data-path collective); the timed region is bracketed by a
+barrier + synchronize and the max over ranks is taken.
 
 --impl reference times the CPU oracle (the plain sequential C coder, spread
 over the host's cores by chunk range) on the same workload and metric.
@@ -27,9 +34,12 @@ import time
 ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
-METRIC = "GPULZ encode+decode round-trip throughput (uncompressed GB/s)"
+METRIC = "GPULZ encode/decode GB/s (uncompressed), ratio; fraction of GB300 HBM roofline"
+VALUE_IS = ("round trip: uncompressed bytes / (encode + decode time), decimal GB/s; "
+            "encode_gbs, decode_gbs, ratio and roofline fractions alongside")
 UNIT = "GB/s"
-CFG_ID = 2
+CFG_ID = 4
+PER_CONFIG = (1, 2, 3, 4, 5)
 L2_FLUSH_BYTES = 256 << 20  # > 129 MB L2
 FALLBACK_HBM_GBS = 6800.0
 
@@ -47,6 +57,9 @@ def parse_args():
     p.add_argument("--config", type=int, default=CFG_ID)
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-e2e", action="store_true")
+    p.add_argument("--no-per-config", action="store_true",
+                   help="skip the per-workload table (configs 1-5)")
+    p.add_argument("--per-config-steps", type=int, default=10)
     p.add_argument("--window", type=int, default=32,
                    help="exact near window in elements (32..64; above 32 on level-0 workloads)")
     p.add_argument("--split", action="store_true",
@@ -71,7 +84,7 @@ def workload_config(cfg, window=32):
         "chunk_size": cfg.chunk_size,
         "match_level": cfg.match_level,
         "seed": cfg.seed,
-        "l2": "flushed between timed steps (256 MB write)",
+        "l2": "flushed before every timed encode and every timed decode (256 MB write)",
     }
 
 
@@ -218,8 +231,131 @@ def cpu_baseline(x, cfg, reps=3, window=32):
 # ----------------------------------------------------------------------------
 # our arm
 # ----------------------------------------------------------------------------
+class Workload:
+    """Device buffers of one workload and its timed encode/decode calls."""
+
+    def __init__(self, g, cfg, x, dev, stream, window=32):
+        import torch
+        self.g, self.cfg, self.x, self.window = g, cfg, x, window
+        self.n = x.size
+        self.stream = stream
+        self.sh = stream.cuda_stream
+        self.d_in = torch.from_numpy(x).to(dev)
+        self.cap = g.gpulz_compress_bound(self.n, cfg.word_size, cfg.chunk_size)
+        self.out = torch.empty(self.cap, dtype=torch.uint8, device=dev)
+        self.nb = torch.zeros(1, dtype=torch.int64, device=dev)
+        self.y = torch.empty(max(self.n, 1), dtype=torch.uint8, device=dev)
+
+    def compress(self):
+        g, c = self.g, self.cfg
+        if self.window == 32:
+            st = g.gpulz_compress(self.d_in, self.n, c.word_size, c.chunk_size, c.match_level,
+                                  self.out, self.cap, self.nb, self.sh)
+        else:
+            st = g.gpulz_compress_window(self.d_in, self.n, c.word_size, c.chunk_size,
+                                         c.match_level, self.window, self.out, self.cap, self.nb,
+                                         self.sh)
+        assert st == g.GPULZ_OK, st
+
+    def decompress(self):
+        assert self.g.gpulz_decompress(self.out, self.y, self.n, self.sh) == self.g.GPULZ_OK
+
+    def timed(self, K, flush, kernel_events=False):
+        """K encode + decode calls, L2 flushed (outside the events) before each
+        call. Per call, CUDA events on the launching stream bracket either the
+        whole library call or, with kernel_events, only its encode or decode
+        kernel (events the library records around that launch)."""
+        import torch
+        g, stream = self.g, self.stream
+        ev = [tuple(torch.cuda.Event(enable_timing=True) for _ in range(4)) for _ in range(K)]
+        for q in ev:
+            for e in q:
+                e.record(stream)  # creates the event
+        torch.cuda.synchronize()
+        for k in range(K):
+            flush.fill_(k & 0xFF)
+            if kernel_events:
+                g.gpulz_set_kernel_events(ev[k][0], ev[k][1])
+            else:
+                ev[k][0].record(stream)
+            self.compress()
+            if not kernel_events:
+                ev[k][1].record(stream)
+            flush.fill_((k + 1) & 0xFF)
+            if kernel_events:
+                g.gpulz_set_kernel_events(ev[k][2], ev[k][3])
+            else:
+                ev[k][2].record(stream)
+            self.decompress()
+            if not kernel_events:
+                ev[k][3].record(stream)
+        g.gpulz_set_kernel_events(None, None)
+        torch.cuda.synchronize()
+        return ([q[0].elapsed_time(q[1]) for q in ev], [q[2].elapsed_time(q[3]) for q in ev])
+
+    def parity(self, threads):
+        """The stream and the decoded bytes of the last call against the oracle."""
+        import numpy as np
+        import oracle
+        c = self.cfg
+        S = int(self.nb.item())
+        got = self.out[:S].cpu().numpy()
+        ref = oracle.compress_threads(self.x, c.word_size, c.chunk_size, c.match_level, threads,
+                                      window=self.window)
+        ok = np.array_equal(got, ref) and np.array_equal(self.y[:self.n].cpu().numpy(), self.x)
+        return ok, S
+
+
+def hbm_fraction(alg_bytes, ms, peak):
+    gbs = alg_bytes / (ms * 1e-3) / 1e9
+    return round(gbs, 2), round(gbs / peak, 4)
+
+
+def per_config_table(g, dev, stream, flush, steps, threads, peak, have=None):
+    """Every workload of PER_CONFIG timed like the headline one (L2 flushed
+    before each call; whole calls and kernels alone) and checked against the
+    oracle; `have` maps a config id to an already measured row."""
+    import synth
+    rows = {}
+    for cid in PER_CONFIG:
+        if have and cid in have:
+            rows[str(cid)] = have[cid]
+            continue
+        cfg = synth.CONFIGS[cid]
+        x = synth.generate(cid)
+        w = Workload(g, cfg, x, dev, stream)
+        for _ in range(3):
+            w.compress()
+            w.decompress()
+        t_enc, t_dec = w.timed(steps, flush)
+        k_enc, k_dec = w.timed(steps, flush, kernel_events=True)
+        status = g.gpulz_device_status(w.sh)
+        ok, S = w.parity(threads)
+        rows[str(cid)] = config_row(cfg, w.n, S, t_enc, t_dec, k_enc, k_dec, peak,
+                                    ok and status == 0)
+        del w
+    return rows
+
+
+def config_row(cfg, n, S, t_enc, t_dec, k_enc, k_dec, peak, ok):
+    enc_ms, dec_ms = statistics.mean(t_enc), statistics.mean(t_dec)
+    ek, dk = statistics.mean(k_enc), statistics.mean(k_dec)
+    return {
+        "workload": cfg.name, "n_bytes": n, "word_size": cfg.word_size,
+        "chunk_size": cfg.chunk_size, "match_level": cfg.match_level,
+        "ratio": round(n / S, 4), "stream_bytes": S,
+        "encode_gbs": round(n / (enc_ms * 1e-3) / 1e9, 2),
+        "decode_gbs": round(n / (dec_ms * 1e-3) / 1e9, 2),
+        "round_trip_gbs": round(n / ((enc_ms + dec_ms) * 1e-3) / 1e9, 2),
+        "encode_kernel_ms": round(ek, 5), "decode_kernel_ms": round(dk, 5),
+        "encode_kernel_hbm_frac": hbm_fraction(n + S, ek, peak)[1],
+        "decode_kernel_hbm_frac": hbm_fraction(S + n, dk, peak)[1],
+        "parity": "bit-exact vs oracle" if ok else "MISMATCH",
+        "steps": len(t_enc),
+    }
+
+
 def run_ours(args):
-    import numpy as np
     import torch
     import torch.distributed as dist
 
@@ -233,88 +369,44 @@ def run_ours(args):
     dev = torch.device("cuda", local)
     g.load()  # raises if the CUDA library is missing: no fallback
     cfg = synth.CONFIGS[args.config]
-    ws, cs, lvl = cfg.word_size, cfg.chunk_size, cfg.match_level
     x = synth.generate(cfg)
-    n = x.size
-    d_in = torch.from_numpy(x).to(dev)
-    cap = g.gpulz_compress_bound(n, ws, cs)
-    out = torch.empty(cap, dtype=torch.uint8, device=dev)
-    nb = torch.zeros(1, dtype=torch.int64, device=dev)
-    y = torch.empty(n, dtype=torch.uint8, device=dev)
-    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream(dev)
-    sh = stream.cuda_stream
     W = args.window
-
-    def compress_call():
-        if W == 32:
-            return g.gpulz_compress(d_in, n, ws, cs, lvl, out, cap, nb, sh)
-        return g.gpulz_compress_window(d_in, n, ws, cs, lvl, W, out, cap, nb, sh)
-
-    def step():
-        st = compress_call()
-        assert st == g.GPULZ_OK, st
-        st = g.gpulz_decompress(out, y, n, sh)
-        assert st == g.GPULZ_OK, st
+    wl = Workload(g, cfg, x, dev, stream, window=W)
+    n, sh = wl.n, wl.sh
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    threads = os.cpu_count() or 1
 
     for _ in range(max(args.warmup, 3)):
         flush.fill_(1)
-        step()
+        wl.compress()
+        flush.fill_(2)
+        wl.decompress()
     assert g.gpulz_device_status(sh) == g.GPULZ_OK
     torch.cuda.synchronize()
 
     K = args.steps
-    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True),
-           torch.cuda.Event(enable_timing=True)) for _ in range(K)]
-    # events the library records right around its encode and decode kernels
-    # (gpulz_set_kernel_events), so that the main kernels are timed alone
-    kev = [tuple(torch.cuda.Event(enable_timing=True) for _ in range(4)) for _ in range(K)]
-    for q in kev:
-        for e in q:
-            e.record(stream)  # creates the event
-    torch.cuda.synchronize()
     if world > 1:
         dist.barrier()
     torch.cuda.synchronize()
     with ClockSampler(local) as clocks:
-        for k in range(K):
-            flush.fill_(k & 0xFF)  # evict the input from L2 (outside the events)
-            ev[k][0].record(stream)
-            assert compress_call() == g.GPULZ_OK
-            ev[k][1].record(stream)
-            assert g.gpulz_decompress(out, y, n, sh) == g.GPULZ_OK
-            ev[k][2].record(stream)
-        torch.cuda.synchronize()
+        t_enc, t_dec = wl.timed(K, flush)
     if world > 1:
         dist.barrier()
-    t_enc = [a.elapsed_time(b) for a, b, c in ev]
-    t_dec = [b.elapsed_time(c) for a, b, c in ev]
     # the main kernels alone: a second run of K steps in which the library
     # records events right around its encode and decode kernels (kept out of
     # the run above so that the extra records cannot perturb `value`)
-    for k in range(K):
-        flush.fill_(k & 0xFF)
-        g.gpulz_set_kernel_events(kev[k][0], kev[k][1])
-        assert compress_call() == g.GPULZ_OK
-        g.gpulz_set_kernel_events(kev[k][2], kev[k][3])
-        assert g.gpulz_decompress(out, y, n, sh) == g.GPULZ_OK
-    g.gpulz_set_kernel_events(None, None)
-    torch.cuda.synchronize()
-    t_enc_kernel = [q[0].elapsed_time(q[1]) for q in kev]
-    t_dec_kernel = [q[2].elapsed_time(q[3]) for q in kev]
+    k_enc, k_dec = wl.timed(K, flush, kernel_events=True)
     total_ms = sum(t_enc) + sum(t_dec)
     if world > 1:
         total_ms = max_over_ranks(total_ms, dist, dev)
     status = g.gpulz_device_status(sh)
 
     # parity after timing, on the same buffers
-    S = int(nb.item())
-    stream_host = out[:S].cpu().numpy()
     parity = "unchecked"
+    S = int(wl.nb.item())
     if rank == 0:
-        import oracle
-        ref = oracle.compress_threads(x, ws, cs, lvl, os.cpu_count() or 1, window=W)
-        ok = np.array_equal(stream_host, ref) and np.array_equal(y.cpu().numpy(), x)
+        ok, S = wl.parity(threads)
         parity = "bit-exact vs oracle" if ok and status == 0 else "MISMATCH"
 
     # end to end through the C ABI with host buffers
@@ -322,20 +414,20 @@ def run_ours(args):
     if not args.no_e2e:
         h_x = torch.from_numpy(x).pin_memory()
         h_nb = torch.zeros(1, dtype=torch.int64).pin_memory()
-        h_s = torch.empty(cap, dtype=torch.uint8).pin_memory()
+        h_s = torch.empty(wl.cap, dtype=torch.uint8).pin_memory()
         h_y = torch.empty(n, dtype=torch.uint8).pin_memory()
-        d_s = torch.empty(cap, dtype=torch.uint8, device=dev)
+        d_s = torch.empty(wl.cap, dtype=torch.uint8, device=dev)
 
         def e2e_step():
-            d_in.copy_(h_x, non_blocking=True)
-            assert compress_call() == g.GPULZ_OK
-            h_nb.copy_(nb, non_blocking=True)
+            wl.d_in.copy_(h_x, non_blocking=True)
+            wl.compress()
+            h_nb.copy_(wl.nb, non_blocking=True)
             stream.synchronize()
             s_len = int(h_nb[0])
-            h_s[:s_len].copy_(out[:s_len], non_blocking=True)
+            h_s[:s_len].copy_(wl.out[:s_len], non_blocking=True)
             d_s[:s_len].copy_(h_s[:s_len], non_blocking=True)
-            assert g.gpulz_decompress(d_s, y, n, sh) == g.GPULZ_OK
-            h_y.copy_(y, non_blocking=True)
+            assert g.gpulz_decompress(d_s, wl.y, n, sh) == g.GPULZ_OK
+            h_y.copy_(wl.y[:n], non_blocking=True)
             stream.synchronize()
             return s_len
 
@@ -356,47 +448,54 @@ def run_ours(args):
         e2e = {"value": round(world * n * K / t_e2e / 1e9, 3), "unit": UNIT,
                "h2d_bytes_per_step": n + s_len, "d2h_bytes_per_step": 8 + s_len + n,
                "path": "pinned host -> gpulz_compress -> host stream -> gpulz_decompress -> host"}
+        del h_x, h_s, h_y, d_s
 
     if rank != 0:
         if world > 1:
             dist.destroy_process_group()
         return
 
-    enc_ms = statistics.mean(t_enc)
-    dec_ms = statistics.mean(t_dec)
-    enc_k_ms = statistics.mean(t_enc_kernel)
-    dec_k_ms = statistics.mean(t_dec_kernel)
     peak, peak_kind = measured_peak()
     alu_peak, alu_src = alu_peak_tops(dev)
-    elems = n // ws
-    enc_ops = W * elems  # near-window equality compares: one per element and offset
-    enc_alg = n + S       # bytes: input read + blocks written (to their slots)
+    enc_ms, dec_ms = statistics.mean(t_enc), statistics.mean(t_dec)
+    enc_k_ms, dec_k_ms = statistics.mean(k_enc), statistics.mean(k_dec)
+    enc_alg = n + S       # bytes: input read + stream written
     dec_alg = S + n       # bytes: stream read + output written
-    enc_s, dec_s = enc_k_ms * 1e-3, dec_k_ms * 1e-3
+    enc_ach, enc_frac = hbm_fraction(enc_alg, enc_k_ms, peak)
+    dec_ach, dec_frac = hbm_fraction(dec_alg, dec_k_ms, peak)
+    enc_ops = W * (n // cfg.word_size)  # near-window equality compares
+    traffic = recorded_traffic("encode_kernel", cfg.name)
     roofline = {
         "kernel": "encode_kernel (timed alone: events the library records around its launch)",
-        "bound": "alu",
-        "achieved": round(enc_ops / enc_s / 1e12, 4),
-        "peak": round(alu_peak, 3),
-        "unit": "Tops/s",
-        "frac": round(enc_ops / enc_s / 1e12 / alu_peak, 4),
-        "peak_source": alu_src,
-        "algorithmic_ops_per_launch": enc_ops,
+        "bound": "hbm",
+        "achieved": enc_ach,
+        "peak": peak,
+        "unit": "GB/s",
+        "frac": enc_frac,
+        "peak_source": peak_kind + " (MEASURED_PEAKS.json hbm_gbs, burst copy)",
+        "alg_bytes_per_launch": enc_alg,
+        "alg_bytes_rule": "input bytes read + stream bytes written",
         "kernel_ms": round(enc_k_ms, 5),
-        "traffic": recorded_traffic("encode_kernel", cfg.name),
-        "hbm": {"achieved": round(enc_alg / enc_s / 1e9, 2), "peak": peak, "unit": "GB/s",
-                "frac": round(enc_alg / enc_s / 1e9 / peak, 4), "alg_bytes": enc_alg,
-                "peak_source": peak_kind + " (MEASURED_PEAKS.json hbm_gbs, burst copy)"},
+        "traffic": traffic,
+        "traffic_source": ("recorded: ncu dram__bytes_read.sum + dram__bytes_write.sum of this "
+                           "kernel source on this workload (profiles/traffic.json)"
+                           if traffic is not None else None),
+        "alu_issue": {"achieved": round(enc_ops / (enc_k_ms * 1e-3) / 1e12, 4),
+                      "peak": round(alu_peak, 3), "unit": "T compares/s",
+                      "frac": round(enc_ops / (enc_k_ms * 1e-3) / 1e12 / alu_peak, 4),
+                      "peak_source": "warp-instruction issue rate: " + alu_src,
+                      "ops_per_launch": enc_ops,
+                      "ops_rule": "%d equality compares per element" % W},
         "decode": {"kernel": "decode_kernel (timed alone, same way)",
                    "bound": "hbm", "kernel_ms": round(dec_k_ms, 5), "alg_bytes": dec_alg,
-                   "achieved": round(dec_alg / dec_s / 1e9, 2), "peak": peak, "unit": "GB/s",
-                   "frac": round(dec_alg / dec_s / 1e9 / peak, 4),
+                   "achieved": dec_ach, "peak": peak, "unit": "GB/s", "frac": dec_frac,
                    "traffic": recorded_traffic("decode_kernel", cfg.name)},
         "encode_pass_ms": round(enc_ms, 5),
         "decode_pass_ms": round(dec_ms, 5),
     }
     line = {
         "metric": METRIC,
+        "value_is": VALUE_IS,
         "value": round(world * n * K / (total_ms * 1e-3) / 1e9, 3),
         "unit": UNIT,
         "n_gpus": world,
@@ -420,6 +519,12 @@ def run_ours(args):
         "clocks": clocks.summary(),
         "e2e": e2e,
     }
+    if not args.no_per_config and world == 1 and W == 32:
+        have = {args.config: config_row(cfg, n, S, t_enc, t_dec, k_enc, k_dec, peak,
+                                        parity == "bit-exact vs oracle")}
+        del wl
+        line["per_config"] = per_config_table(g, dev, stream, flush, args.per_config_steps,
+                                              threads, peak, have)
     if not args.no_cpu_baseline and world == 1:
         line["cpu_baseline"] = cpu_baseline(x, cfg, window=W)
     print(json.dumps(line), flush=True)
@@ -459,6 +564,7 @@ def run_reference(args):
     line = {
         "impl": "reference",
         "metric": METRIC,
+        "value_is": VALUE_IS,
         "value": value,
         "unit": UNIT,
         "n_gpus": world,
