@@ -60,6 +60,8 @@ def parse_args():
     p.add_argument("--no-per-config", action="store_true",
                    help="skip the per-workload table (configs 1-5)")
     p.add_argument("--per-config-steps", type=int, default=10)
+    p.add_argument("--max-bytes", type=int, default=0,
+                   help="code only the first N bytes of the workload (smaller profiling cases)")
     p.add_argument("--window", type=int, default=32,
                    help="exact near window in elements (32..64; above 32 on level-0 workloads)")
     p.add_argument("--split", action="store_true",
@@ -74,12 +76,14 @@ def dist_env():
     return world, rank, local
 
 
-def workload_config(cfg, window=32):
+def workload_config(cfg, window=32, n_bytes=None):
     extra = {} if window == 32 else {"near_window": window}
+    if n_bytes is not None and n_bytes != cfg.n_bytes:
+        extra["first_bytes_only"] = n_bytes
     return extra | {
         "workload": cfg.name,
         "field": "x".join(str(s) for s in cfg.shape) + " float32 sinusoids+noise, " + cfg.codes,
-        "n_bytes": cfg.n_bytes,
+        "n_bytes": cfg.n_bytes if n_bytes is None else n_bytes,
         "word_size": cfg.word_size,
         "chunk_size": cfg.chunk_size,
         "match_level": cfg.match_level,
@@ -370,6 +374,8 @@ def run_ours(args):
     g.load()  # raises if the CUDA library is missing: no fallback
     cfg = synth.CONFIGS[args.config]
     x = synth.generate(cfg)
+    if args.max_bytes:
+        x = x[: args.max_bytes].copy()
     stream = torch.cuda.current_stream(dev)
     W = args.window
     wl = Workload(g, cfg, x, dev, stream, window=W)
@@ -507,7 +513,7 @@ def run_ours(args):
         "vs_baseline": None,
         "dtype": cfg.dtype,
         "data": "synthetic (seeded stand-in for Lorenzo-quantized CLDHGH residuals)",
-        "config": workload_config(cfg, W),
+        "config": workload_config(cfg, W, n),
         "encode_gbs": round(n / (enc_ms * 1e-3) / 1e9, 2),
         "decode_gbs": round(n / (dec_ms * 1e-3) / 1e9, 2),
         "ratio": round(n / S, 4),
@@ -519,7 +525,7 @@ def run_ours(args):
         "clocks": clocks.summary(),
         "e2e": e2e,
     }
-    if not args.no_per_config and world == 1 and W == 32:
+    if not args.no_per_config and world == 1 and W == 32 and not args.max_bytes:
         have = {args.config: config_row(cfg, n, S, t_enc, t_dec, k_enc, k_dec, peak,
                                         parity == "bit-exact vs oracle")}
         del wl

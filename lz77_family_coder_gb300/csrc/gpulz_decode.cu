@@ -299,8 +299,16 @@ __device__ void decode_chunks(const DecodeArgs& a, const Geo& g, uint8_t* slot_b
         }
 
         // ---- D4: scatter literals and back-pointers ----
+        // Bytes (4096-element chunks, long lane ranges): element q + k of a
+        // match copies element q + k - O, which has the value of element
+        // q - O + (k mod O); when that element lies in this lane's own range,
+        // its entry is already final (a literal, or a pointer into an earlier
+        // lane's range) and is copied, so pointer jumping only follows
+        // pointers that cross lane ranges (about half the rounds there; for
+        // wider words the extra load costs more than the rounds it saves).
         bool lane_bad = false;
-        uint32_t q = incl - span_sum;
+        const uint32_t q_lane = incl - span_sum;  // first position of this lane's items
+        uint32_t q = q_lane;
         for (uint32_t j = j_lo; j < j_hi; ++j) {
             uint32_t w = s_fl[j >> 5];
             bool ism = (w >> (j & 31u)) & 1u;
@@ -315,7 +323,17 @@ __device__ void decode_chunks(const DecodeArgs& a, const Geo& g, uint8_t* slot_b
                     lane_bad = true;
                     break;
                 }
-                for (uint32_t k = 0; k < L; ++k) s_src[q + k] = (uint16_t)(q + k - O);
+                if (WS == 1) {
+                    const uint32_t s0 = q - O;
+                    uint32_t r = 0;
+                    for (uint32_t k = 0; k < L; ++k) {
+                        const uint32_t t = s0 + r;
+                        s_src[q + k] = t >= q_lane ? s_src[t] : (uint16_t)t;
+                        r = r + 1u == O ? 0u : r + 1u;
+                    }
+                } else {
+                    for (uint32_t k = 0; k < L; ++k) s_src[q + k] = (uint16_t)(q + k - O);
+                }
                 q += L;
             } else {
                 s_src[q] = (uint16_t)(kLit | b);

@@ -907,36 +907,61 @@ __global__ void __launch_bounds__(256, 4) encode_kernel(EncodeArgs a) {
                     if (tid == 0)
                         for (uint32_t z = dbytes; z < ((dbytes + 3u) & ~3u); ++z) s_data[z] = 0;
                 }
-                uint32_t fbits = 0, k = 0, rem = a.split ? 0u : path;
-                while (rem) {
-                    const uint32_t p = (uint32_t)__ffs(rem) - 1u;
-                    rem &= rem - 1u;
-                    const uint32_t pos = seg_a + p;
-                    if ((mmask >> p) & 1u) {
-                        const uint32_t lo = s_lo[pos];
-                        if (WS == 1) {
-                            s_data[bb] = (uint8_t)lo;
-                            s_data[bb + 1] = (uint8_t)(lo >> 8);
-                        } else {
-                            *reinterpret_cast<uint16_t*>(s_data + bb) = (uint16_t)lo;
-                        }
-                        bb += 2u;
-                        fbits |= 1u << k;
-                    } else {
-                        const uint32_t v = el_get<WS>(s_el, pos);
-                        if (WS == 1) {
-                            s_data[bb] = (uint8_t)v;
-                        } else if (WS == 2) {
-                            *reinterpret_cast<uint16_t*>(s_data + bb) = (uint16_t)v;
-                        } else {
-                            *reinterpret_cast<uint16_t*>(s_data + bb) = (uint16_t)v;
-                            *reinterpret_cast<uint16_t*>(s_data + bb + 2) = (uint16_t)(v >> 16);
-                        }
-                        bb += WS;
-                    }
-                    ++k;
-                }
                 if (!a.split) {
+                    // the segment's tokens and elements in registers (vector
+                    // loads), then its items written position by position
+                    // (predicated, no loop over a data-dependent count)
+                    uint32_t lo[SEGP / 2];
+                    {
+                        const uint4* q = reinterpret_cast<const uint4*>(s_lo + seg_a);
+#pragma unroll
+                        for (int h = 0; h < SEGP / 8; ++h) {
+                            const uint4 v = q[h];
+                            lo[4 * h] = v.x; lo[4 * h + 1] = v.y; lo[4 * h + 2] = v.z; lo[4 * h + 3] = v.w;
+                        }
+                    }
+                    constexpr int NW = SEGP * WS / 4;  // words holding the segment's elements
+                    uint32_t ew[NW];
+                    {
+                        const uint8_t* e0 = s_el + el_addr<WS>(seg_a);
+                        if (NW >= 4) {
+#pragma unroll
+                            for (int h = 0; h < NW / 4; ++h) {
+                                const uint4 v = reinterpret_cast<const uint4*>(e0)[h];
+                                ew[4 * h] = v.x; ew[4 * h + 1] = v.y; ew[4 * h + 2] = v.z; ew[4 * h + 3] = v.w;
+                            }
+                        } else {
+                            const uint2 v = *reinterpret_cast<const uint2*>(e0);
+                            ew[0] = v.x; ew[NW - 1] = v.y;
+                        }
+                    }
+                    uint32_t fbits = 0, k = 0;
+#pragma unroll
+                    for (int p = 0; p < SEGP; ++p) {
+                        if (!((path >> p) & 1u)) continue;
+                        if ((mmask >> p) & 1u) {
+                            const uint32_t v = (lo[p >> 1] >> (16 * (p & 1))) & 0xFFFFu;
+                            if (WS == 1) {
+                                s_data[bb] = (uint8_t)v;
+                                s_data[bb + 1] = (uint8_t)(v >> 8);
+                            } else {
+                                *reinterpret_cast<uint16_t*>(s_data + bb) = (uint16_t)v;
+                            }
+                            bb += 2u;
+                            fbits |= 1u << k;
+                        } else {
+                            if (WS == 1) {
+                                s_data[bb] = (uint8_t)(ew[p >> 2] >> (8 * (p & 3)));
+                            } else if (WS == 2) {
+                                *reinterpret_cast<uint16_t*>(s_data + bb) = (uint16_t)(ew[p >> 1] >> (16 * (p & 1)));
+                            } else {
+                                *reinterpret_cast<uint16_t*>(s_data + bb) = (uint16_t)ew[p];
+                                *reinterpret_cast<uint16_t*>(s_data + bb + 2) = (uint16_t)(ew[p] >> 16);
+                            }
+                            bb += WS;
+                        }
+                        ++k;
+                    }
                     if (fbits) or_bits(s_fl, item_base, fbits);
                     if (tid == 0)
                         for (uint32_t z = dbytes; z < ((dbytes + 3u) & ~3u); ++z) s_data[z] = 0;
