@@ -411,6 +411,16 @@ __global__ void __launch_bounds__(256, 4) encode_kernel(EncodeArgs a) {
     // predecessors have published their sizes, so the wait is normally empty.
     uint32_t p_c = NONE, p_blk = 0, p_entry = 0, p_dbytes = 0, p_fw = 0, p_dw = 0;
 
+    // Level-1 bucket entries are (tag << 16) | (position + 1), the tag counting
+    // this CTA's chunks: an entry left by an earlier chunk has a smaller tag,
+    // so it loses every atomicMax and reads as empty, and the table is cleared
+    // only here (visible after the barrier that follows the first ticket) and
+    // when the 16-bit tag wraps.
+    uint32_t tag = 0;
+    if (LEVEL) {
+        for (uint32_t k = tid; k < 2u * E; k += nthreads) s_tab[k] = 0;
+    }
+
     for (;;) {
         if (tid == 0) s_misc[0] = atomicAdd(a.ticket, 1u);
         __syncthreads();
@@ -451,7 +461,10 @@ __global__ void __launch_bounds__(256, 4) encode_kernel(EncodeArgs a) {
                 }
             }
             if (LEVEL) {
-                for (uint32_t k = tid; k < 2u * E; k += nthreads) s_tab[k] = 0;
+                if (++tag == 0x10000u) {
+                    for (uint32_t k = tid; k < 2u * E; k += nthreads) s_tab[k] = 0;
+                    tag = 1;
+                }
             }
             // ---- E2: zero test ----
             nonzero = __syncthreads_or(nz != 0) != 0;
@@ -638,8 +651,8 @@ __global__ void __launch_bounds__(256, 4) encode_kernel(EncodeArgs a) {
                                 s_hk[i] = (uint16_t)h;
                                 if (s > 0) {
                                     const uint32_t slot = s_tab[h];
-                                    d = i + 1u - slot;  // i - p for p = slot - 1
-                                    if (slot == 0u || d <= 32u || d > (uint32_t)kMaxOff) d = 0;
+                                    d = i + 1u - (slot & 0xFFFFu);  // i - p for p = slot - 1
+                                    if ((slot >> 16) != tag || d <= 32u || d > (uint32_t)kMaxOff) d = 0;
                                 }
                             }
                             s_cd[i] = (uint8_t)d;
@@ -647,7 +660,7 @@ __global__ void __launch_bounds__(256, 4) encode_kernel(EncodeArgs a) {
                         __syncthreads();
                         if (s + 1 < kSubBlocks) {
                             for (uint32_t p = lo_i + tid; p < lo_i + SB; p += nthreads)
-                                if (p + 1u < E) atomicMax(&s_tab[s_hk[p]], p + 1u);
+                                if (p + 1u < E) atomicMax(&s_tab[s_hk[p]], (tag << 16) | (p + 1u));
                             __syncthreads();
                         }
                     }
