@@ -625,19 +625,21 @@ def run_split(args):
         assert g.gpulz_decompress_split(*ports, plen, y, n, sh) == g.GPULZ_OK
     assert g.gpulz_device_status(sh) == g.GPULZ_OK
     K = args.steps
-    ev = [tuple(torch.cuda.Event(enable_timing=True) for _ in range(3)) for _ in range(K)]
     torch.cuda.synchronize()
+    ev = [tuple(torch.cuda.Event(enable_timing=True) for _ in range(4)) for _ in range(K)]
     with ClockSampler(0) as clocks:
         for k in range(K):
             flush.fill_(k & 0xFF)
             ev[k][0].record(stream)
             assert g.gpulz_compress_split(d_in, n, ws, cs, lvl, *ports, caps, pb, sh) == g.GPULZ_OK
             ev[k][1].record(stream)
-            assert g.gpulz_decompress_split(*ports, plen, y, n, sh) == g.GPULZ_OK
+            flush.fill_((k + 1) & 0xFF)
             ev[k][2].record(stream)
+            assert g.gpulz_decompress_split(*ports, plen, y, n, sh) == g.GPULZ_OK
+            ev[k][3].record(stream)
         torch.cuda.synchronize()
-    t_enc = [a.elapsed_time(b) for a, b, c in ev]
-    t_dec = [b.elapsed_time(c) for a, b, c in ev]
+    t_enc = [q[0].elapsed_time(q[1]) for q in ev]
+    t_dec = [q[2].elapsed_time(q[3]) for q in ev]
     status = g.gpulz_device_status(sh)
     import oracle
     ref = oracle.compress_split(x, ws, cs, lvl)
