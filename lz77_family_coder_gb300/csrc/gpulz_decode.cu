@@ -274,16 +274,33 @@ __device__ void decode_chunks(const DecodeArgs& a, const Geo& g, uint8_t* slot_b
         const uint32_t K = (items + 31u) / 32u;
         const uint32_t j_lo = lane * K < items ? lane * K : items;
         const uint32_t j_hi = j_lo + K < items ? j_lo + K : items;
+        // Wider words in a single stream: the lane keeps its flag word and its
+        // match count in registers and reads each item's two bytes with one
+        // 16-bit load (every item starts at an even byte), with no branch
+        // between literals and matches. Bytes and split mode: per item.
+        const bool uni = WS != 1 && !split;
         uint32_t span_sum = 0;
-        for (uint32_t j = j_lo; j < j_hi; ++j) {
-            uint32_t w = s_fl[j >> 5];
-            bool ism = (w >> (j & 31u)) & 1u;
-            if (ism) {
-                uint32_t pm = s_wp[j >> 5] + __popc(w & ((1u << (j & 31u)) - 1u));
-                uint32_t b = split ? slit + pm : WS * j - (WS - 2u) * pm;
-                span_sum += s_data[b];
-            } else {
-                span_sum += 1u;
+        if (uni) {
+            uint32_t w = j_lo < j_hi ? s_fl[j_lo >> 5] : 0u;
+            uint32_t pm = j_lo < j_hi ? s_wp[j_lo >> 5] + __popc(w & ((1u << (j_lo & 31u)) - 1u)) : 0u;
+            for (uint32_t j = j_lo; j < j_hi; ++j) {
+                if ((j & 31u) == 0u) w = s_fl[j >> 5];
+                const uint32_t ism = (w >> (j & 31u)) & 1u;
+                const uint32_t tok = *reinterpret_cast<const uint16_t*>(s_data + (WS * j - (WS - 2u) * pm));
+                span_sum += ism ? (tok & 0xFFu) : 1u;
+                pm += ism;
+            }
+        } else {
+            for (uint32_t j = j_lo; j < j_hi; ++j) {
+                uint32_t w = s_fl[j >> 5];
+                bool ism = (w >> (j & 31u)) & 1u;
+                if (ism) {
+                    uint32_t pm = s_wp[j >> 5] + __popc(w & ((1u << (j & 31u)) - 1u));
+                    uint32_t b = split ? slit + pm : WS * j - (WS - 2u) * pm;
+                    span_sum += s_data[b];
+                } else {
+                    span_sum += 1u;
+                }
             }
         }
         uint32_t incl = span_sum;
@@ -309,7 +326,28 @@ __device__ void decode_chunks(const DecodeArgs& a, const Geo& g, uint8_t* slot_b
         bool lane_bad = false;
         const uint32_t q_lane = incl - span_sum;  // first position of this lane's items
         uint32_t q = q_lane;
-        for (uint32_t j = j_lo; j < j_hi; ++j) {
+        if (uni) {
+            // entries v0, v0 + 1, ... for a match (q - O onwards), one kLit | b
+            // entry for a literal
+            uint32_t w = j_lo < j_hi ? s_fl[j_lo >> 5] : 0u;
+            uint32_t pm = j_lo < j_hi ? s_wp[j_lo >> 5] + __popc(w & ((1u << (j_lo & 31u)) - 1u)) : 0u;
+            for (uint32_t j = j_lo; j < j_hi; ++j) {
+                if ((j & 31u) == 0u) w = s_fl[j >> 5];
+                const uint32_t ism = (w >> (j & 31u)) & 1u;
+                const uint32_t b = WS * j - (WS - 2u) * pm;
+                const uint32_t tok = *reinterpret_cast<const uint16_t*>(s_data + b);
+                const uint32_t L = ism ? (tok & 0xFFu) : 1u, O = tok >> 8;
+                if (ism && (L == 0u || O == 0u || O > q)) {
+                    lane_bad = true;
+                    break;
+                }
+                const uint32_t v0 = ism ? q - O : (kLit | b);
+                for (uint32_t k = 0; k < L; ++k) s_src[q + k] = (uint16_t)(v0 + ism * k);
+                q += L;
+                pm += ism;
+            }
+        }
+        for (uint32_t j = uni ? j_hi : j_lo; j < j_hi; ++j) {
             uint32_t w = s_fl[j >> 5];
             bool ism = (w >> (j & 31u)) & 1u;
             uint32_t pm = s_wp[j >> 5] + __popc(w & ((1u << (j & 31u)) - 1u));
