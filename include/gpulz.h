@@ -188,14 +188,15 @@ gpulz_status gpulz_release_scratch(cudaStream_t stream);
  * Limit: at most 65536 chunks per call (256 MiB of input at chunk_size 4096,
  * 128 MiB at 2048, 64 MiB at 1024); larger inputs return
  * GPULZ_ERR_INVALID_ARG and launch nothing.
- * Set-up: the first call on a device looks up the array's device address with
- * that device current; make that first call before any stream capture.
+ * Set-up: the first call on a device looks up the array's device address,
+ * with that device current.
  * Sharing: all calls on a device share the one array, which keeps the last
  * call's contents; each call first clears, on its stream, the part it uses
  * (status word, ticket, one look-back entry per chunk). Calls that overlap on
- * the GPU (other streams, other host threads) race and must not be issued. A device-side wait that gives up
- * sets *d_out_bytes to SIZE_MAX; capacity overflow shows as
- * *d_out_bytes > capacity. gpulz_device_status() does not see this path.
+ * the GPU (other streams, other host threads) race and must not be issued.
+ * A device-side wait that gives up sets *d_out_bytes to SIZE_MAX; capacity
+ * overflow shows as *d_out_bytes > capacity. gpulz_device_status() does not
+ * see this path.
  */
 gpulz_status gpulz_compress_noalloc(const void* d_in, size_t n_bytes, int word_size,
                                     int chunk_size, int match_level, void* d_out,
