@@ -626,47 +626,65 @@ __global__ void __launch_bounds__(256, 4) encode_kernel(EncodeArgs a) {
                 // ---- E5: level-1 hashed candidates over 8 sub-blocks ----
                 // The sub-block phases only look the buckets up and insert;
                 // the candidates are checked afterwards, with no barrier in
-                // between. Bucket and candidate offset of each position live
-                // in the omask area (the masks are dead once E4 is done).
-                // Sub-block 0 finds an empty table and the last sub-block's
-                // inserts are never looked up, so neither is done. A candidate
-                // at offset d <= 32 never wins: the near search already found
-                // the longest run over offsets 1..32 with the same caps,
-                // nearest first. For d > 32 it wins only with a run longer
-                // than the near length l0. In the two-pass kernel the staging
-                // buffer is idle until E7 and holds an unpadded copy of the
-                // chunk (written in E1) for the hashing and the compares.
+                // between. Thread tid owns position s*SB + r*nthreads + tid of
+                // each sub-block s (r < R = SEGP/8, so SB = R*nthreads); the
+                // bucket and candidate offset of an owned position stay in its
+                // registers. Sub-block 0 finds an empty table and the last
+                // sub-block's inserts are never looked up, so neither is done.
+                // A candidate at offset d <= 32 never wins: the near search
+                // already found the longest run over offsets 1..32 with the
+                // same caps, nearest first. For d > 32 it wins only with a run
+                // longer than the near length l0. In the two-pass kernel the
+                // staging buffer is idle until E7 and holds an unpadded copy of
+                // the chunk (written in E1) for the hashing and the compares.
                 if (LEVEL) {
-                    uint16_t* s_hk = reinterpret_cast<uint16_t*>(s_om);
-                    uint8_t* s_cd = reinterpret_cast<uint8_t*>(s_om) + 2u * E;
+                    constexpr int R = SEGP / 8;
+                    constexpr int NP = kSubBlocks * R;
                     const uint32_t SB = E / kSubBlocks;
+                    uint32_t cd[NP / 4];  // candidate offset of owned position j in byte j
+#pragma unroll
+                    for (int w = 0; w < NP / 4; ++w) cd[w] = 0;
+                    uint32_t cm = 0;      // owned positions with a candidate
+#pragma unroll
                     for (int s = 0; s < kSubBlocks; ++s) {
-                        const uint32_t lo_i = (uint32_t)s * SB;
-                        for (uint32_t i = lo_i + tid; i < lo_i + SB; i += nthreads) {
-                            uint32_t d = 0;
-                            if (i + 1u < E) {
-                                const uint32_t h =
-                                    SINGLE ? key_hash(el_get<WS>(s_el, i), el_get<WS>(s_el, i + 1u), a.hash_bits)
-                                           : key_hash(lin_get<WS>(s_data, i), lin_get<WS>(s_data, i + 1u), a.hash_bits);
-                                s_hk[i] = (uint16_t)h;
-                                if (s > 0) {
-                                    const uint32_t slot = s_tab[h];
-                                    d = i + 1u - (slot & 0xFFFFu);  // i - p for p = slot - 1
-                                    if ((slot >> 16) != tag || d <= 32u || d > (uint32_t)kMaxOff) d = 0;
-                                }
-                            }
-                            s_cd[i] = (uint8_t)d;
+                        uint32_t hk[R];
+#pragma unroll
+                        for (int r = 0; r < R; ++r) {
+                            const uint32_t i = (uint32_t)s * SB + (uint32_t)r * (uint32_t)nthreads + (uint32_t)tid;
+                            const uint32_t i1 = i + 1u < E ? i + 1u : i;
+                            hk[r] = SINGLE ? key_hash(el_get<WS>(s_el, i), el_get<WS>(s_el, i1), a.hash_bits)
+                                           : key_hash(lin_get<WS>(s_data, i), lin_get<WS>(s_data, i1), a.hash_bits);
                         }
-                        __syncthreads();
+                        if (s > 0) {
+#pragma unroll
+                            for (int r = 0; r < R; ++r) {
+                                const int j = s * R + r;
+                                const uint32_t i = (uint32_t)s * SB + (uint32_t)r * (uint32_t)nthreads + (uint32_t)tid;
+                                const uint32_t slot = s_tab[hk[r]];
+                                uint32_t d = i + 1u - (slot & 0xFFFFu);  // i - p for p = slot - 1
+                                if ((slot >> 16) != tag || d <= 32u || d > (uint32_t)kMaxOff || i + 1u >= E) d = 0;
+                                cd[j >> 2] |= d << (8 * (j & 3));
+                                cm |= (uint32_t)(d != 0u) << j;
+                            }
+                            if (s + 1 < kSubBlocks) __syncthreads();  // lookups before this sub-block's inserts
+                        }
                         if (s + 1 < kSubBlocks) {
-                            for (uint32_t p = lo_i + tid; p < lo_i + SB; p += nthreads)
-                                if (p + 1u < E) atomicMax(&s_tab[s_hk[p]], (tag << 16) | (p + 1u));
-                            __syncthreads();
+#pragma unroll
+                            for (int r = 0; r < R; ++r) {
+                                const uint32_t i = (uint32_t)s * SB + (uint32_t)r * (uint32_t)nthreads + (uint32_t)tid;
+                                if (i + 1u < E) atomicMax(&s_tab[hk[r]], (tag << 16) | (i + 1u));
+                            }
+                            __syncthreads();  // inserts before the next sub-block's lookups
                         }
                     }
-                    for (uint32_t i = SB + tid; i < E; i += nthreads) {
-                        const uint32_t d = s_cd[i];
-                        if (!d) continue;
+                    while (cm) {
+                        const uint32_t j = (uint32_t)__ffs(cm) - 1u;
+                        cm &= cm - 1u;
+                        uint32_t dw = cd[0];
+#pragma unroll
+                        for (int w = 1; w < NP / 4; ++w) dw = (j >> 2) == (uint32_t)w ? cd[w] : dw;
+                        const uint32_t d = (dw >> (8u * (j & 3u))) & 0xFFu;
+                        const uint32_t i = (j / (uint32_t)R) * SB + (j % (uint32_t)R) * (uint32_t)nthreads + (uint32_t)tid;
                         const uint32_t cap = E - i < (uint32_t)kMaxLen ? E - i : (uint32_t)kMaxLen;
                         const uint32_t l0 = s_lo[i] & 0xFFu;
                         if (l0 >= cap) continue;
@@ -1198,9 +1216,13 @@ cudaError_t launch_t(const EncodeArgs& a, cudaStream_t stream) {
     static thread_local LaunchShape shape16, shape8, shape_copy;
     const EncLayout L = enc_layout(a.chunk_size, a.elems, LEVEL);
     const int threads = 32 * team_warps(a.elems);
-    // positions per thread: 8, except 16 for 4096-element chunks
+    // positions per thread: 8, except 16 for 4096-element chunks (bytes at
+    // chunk_size 4096, the only geometry with that many elements)
     const bool s16 = a.elems / (uint32_t)threads == 16u;
-    auto kern = s16 ? encode_kernel<WS, LEVEL, 16, SINGLE, NEARW> : encode_kernel<WS, LEVEL, 8, SINGLE, NEARW>;
+    void (*kern)(EncodeArgs) = encode_kernel<WS, LEVEL, 8, SINGLE, NEARW>;
+    if constexpr (WS == 1) {
+        if (s16) kern = encode_kernel<WS, LEVEL, 16, SINGLE, NEARW>;
+    }
     LaunchShape& shape = s16 ? shape16 : shape8;
     cudaError_t err = shape_for(kern, threads, L.total, shape);
     if (err != cudaSuccess) return err;
