@@ -159,6 +159,34 @@ __device__ void write_header_split(const EncodeArgs& a, uint32_t ws, uint64_t me
         atomicOr(a.status, kStatCapacity);
 }
 
+// The two steps below are written as predicated PTX because the plain C forms
+// (`mm |= (a == b) ? bit : 0`, and a select of the chain's new mask) compile
+// to a compare, a select and an OR on the integer pipe, which bounds this
+// kernel; the near masks alone are 32 compares per element. Measured, all
+// streams unchanged: near masks +8-18 % encode on every workload, chain steps
+// and verification compares a further +3-10 %.
+//
+// mm |= bit where a == b: one compare and one predicated OR.
+__device__ __forceinline__ void or_if_equal(uint32_t& mm, uint32_t a, uint32_t b, uint32_t bit) {
+    asm("{\n\t.reg .pred q;\n\tsetp.eq.u32 q, %1, %2;\n\t@q or.b32 %0, %0, %3;\n\t}"
+        : "+r"(mm)
+        : "r"(a), "r"(b), "r"(bit));
+}
+
+// One AND-chain step of chain p (bit = 1 << p): x = c & m; where bit p of
+// `live` is set and x != 0, c = x and bit p of `an` is set.
+__device__ __forceinline__ void chain_step(uint32_t& c, uint32_t& an, uint32_t m, uint32_t live, uint32_t bit) {
+    asm("{\n\t.reg .pred q, r;\n\t.reg .b32 x, y;\n\t"
+        "and.b32 x, %0, %2;\n\t"
+        "and.b32 y, %3, %4;\n\t"
+        "setp.ne.u32 r, y, 0;\n\t"
+        "setp.ne.and.u32 q, x, 0, r;\n\t"
+        "@q mov.b32 %0, x;\n\t"
+        "@q or.b32 %1, %1, %4;\n\t}"
+        : "+r"(c), "+r"(an)
+        : "r"(m), "r"(live), "r"(bit));
+}
+
 // ---------------------------------------------------------------------------
 // Per-segment near masks (E3): m[p] bit o-1 set iff element (base+p) equals
 // element (base+p-o), 1 <= o <= 32, base+p-o >= 0.
@@ -196,7 +224,7 @@ __device__ __forceinline__ void near_masks(const uint8_t* s_el, uint32_t base, u
             const uint32_t x = v[32 + p];
             uint32_t mm = 0;
 #pragma unroll
-            for (int o = 1; o <= 32; ++o) mm |= (v[32 + p - o] == x) ? (1u << (o - 1)) : 0u;
+            for (int o = 1; o <= 32; ++o) or_if_equal(mm, v[32 + p - o], x, 1u << (o - 1));
             const uint32_t i = base + (uint32_t)(8 * h + p);
             if (i < 32u) mm &= (1u << i) - 1u;
             m[8 * h + p] = mm;
@@ -263,7 +291,7 @@ __device__ __forceinline__ void near_masks_far(const uint8_t* s_el, uint32_t bas
             const uint32_t x = el_get<WS>(s_el, i);
             uint32_t mm = 0;
 #pragma unroll
-            for (int o = 1; o <= 32; ++o) mm |= (v[p + 32 - o] == x) ? (1u << (o - 1)) : 0u;
+            for (int o = 1; o <= 32; ++o) or_if_equal(mm, v[p + 32 - o], x, 1u << (o - 1));
             if (i < 64u) mm &= i > 32u ? (1u << (i - 32u)) - 1u : 0u;
             m[8 * h + p] = mm & far_mask;
         }
@@ -296,10 +324,7 @@ __device__ __forceinline__ void and_chains(const uint32_t (&m)[SEGP], const uint
         uint32_t An = 0;
 #pragma unroll
         for (int p = 0; p + k < SEGP; ++p) {
-            const uint32_t x = cc[p] & m[p + k];
-            const bool ok = ((act >> p) & 1u) && x != 0u;
-            cc[p] = ok ? x : cc[p];
-            An |= (uint32_t)ok << p;
+            chain_step(cc[p], An, m[p + k], act, 1u << p);
         }
 #pragma unroll
         for (int w = 0; w < SEGP / 4; ++w) lb[w] += expand4((An >> (4 * w)) & 15u);
@@ -339,10 +364,7 @@ __device__ __forceinline__ void and_chains(const uint32_t (&m)[SEGP], const uint
                 uint32_t An = 0;
 #pragma unroll
                 for (int p = 0; p < SEGP; ++p) {
-                    const uint32_t x = cc[p] & om;
-                    const bool ok = ((A2 >> p) & 1u) && x != 0u;
-                    cc[p] = ok ? x : cc[p];
-                    An |= (uint32_t)ok << p;
+                    chain_step(cc[p], An, om, A2, 1u << p);
                 }
 #pragma unroll
                 for (int w = 0; w < SEGP / 4; ++w) lb[w] += expand4((An >> (4 * w)) & 15u);
@@ -508,10 +530,7 @@ __global__ void __launch_bounds__(256, 4) encode_kernel(EncodeArgs a) {
                         uint32_t An = 0;
 #pragma unroll
                         for (int p = 0; p + k < SEGP; ++p) {
-                            const uint32_t x = cc[p] & m[p + k];
-                            const bool ok = ((act >> p) & 1u) && x != 0u;
-                            cc[p] = ok ? x : cc[p];
-                            An |= (uint32_t)ok << p;
+                            chain_step(cc[p], An, m[p + k], act, 1u << p);
                         }
 #pragma unroll
                         for (int w = 0; w < SEGP / 4; ++w) lb[w] += expand4((An >> (4 * w)) & 15u);
@@ -563,10 +582,7 @@ __global__ void __launch_bounds__(256, 4) encode_kernel(EncodeArgs a) {
                                 uint32_t An = 0;
 #pragma unroll
                                 for (int p = 0; p < SEGP; ++p) {
-                                    const uint32_t x = cc[p] & om;
-                                    const bool ok = ((A2 >> p) & 1u) && x != 0u;
-                                    cc[p] = ok ? x : cc[p];
-                                    An |= (uint32_t)ok << p;
+                                    chain_step(cc[p], An, om, A2, 1u << p);
                                 }
 #pragma unroll
                                 for (int w = 0; w < SEGP / 4; ++w) lb[w] += expand4((An >> (4 * w)) & 15u);
@@ -701,7 +717,7 @@ __global__ void __launch_bounds__(256, 4) encode_kernel(EncodeArgs a) {
                                 uint32_t eq = 0;
 #pragma unroll
                                 for (int r = 0; r < 4; ++r)
-                                    eq |= (uint32_t)(lin_at<WS>(pa, k + (uint32_t)r) == lin_at<WS>(pb, k + (uint32_t)r)) << r;
+                                    or_if_equal(eq, lin_at<WS>(pa, k + (uint32_t)r), lin_at<WS>(pb, k + (uint32_t)r), 1u << r);
                                 const uint32_t lead = (uint32_t)__ffs(~eq) - 1u;  // 0..4
                                 k += lead;
                                 if (lead < 4u || k >= cap) break;
