@@ -21,8 +21,9 @@
 // The greedy parse is computed in parallel: each thread walks its own
 // segment from the segment start, then every thread whose true entry (the
 // previous segment's exit) differs re-walks from it until its path meets the
-// old one (paths that meet coincide afterwards); this repeats until no entry
-// changes, which gives exactly the sequential parse.
+// old one (paths that meet coincide afterwards); this repeats until a round
+// changes no exit, when every entry equals the exit before it: exactly the
+// sequential parse.
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -677,10 +678,14 @@ __global__ void __launch_bounds__(256, 4) encode_kernel(EncodeArgs a) {
                                 const int j = s * R + r;
                                 const uint32_t i = (uint32_t)s * SB + (uint32_t)r * (uint32_t)nthreads + (uint32_t)tid;
                                 const uint32_t slot = s_tab[hk[r]];
-                                uint32_t d = i + 1u - (slot & 0xFFFFu);  // i - p for p = slot - 1
-                                if ((slot >> 16) != tag || d <= 32u || d > (uint32_t)kMaxOff || i + 1u >= E) d = 0;
-                                cd[j >> 2] |= d << (8 * (j & 3));
-                                cm |= (uint32_t)(d != 0u) << j;
+                                const uint32_t d = i + 1u - (slot & 0xFFFFu);  // i - p for p = slot - 1
+                                // this chunk's entry (tag), 32 < d <= kMaxOff, a key at i
+                                const bool ok = ((slot ^ (tag << 16)) < 0x10000u) &
+                                                (d - 33u < (uint32_t)(kMaxOff - 32)) & (i + 1u < E);
+                                if (ok) {
+                                    cd[j >> 2] |= d << (8 * (j & 3));
+                                    cm |= 1u << j;
+                                }
                             }
                             if (s + 1 < kSubBlocks) __syncthreads();  // lookups before this sub-block's inserts
                         }
@@ -750,16 +755,19 @@ __global__ void __launch_bounds__(256, 4) encode_kernel(EncodeArgs a) {
                 // step bytes held in registers; then every thread whose true
                 // entry (the previous segment's exit) differs from the entry its
                 // path assumed re-walks from it, keeping its old path from the
-                // first common position on. This repeats until no entry changes.
+                // first common position on. This repeats until a round changes no
+                // exit (then the next round would read the same entries: every
+                // entry equals the exit before it, which only the sequential
+                // parse satisfies; most chunks stop after one round).
                 // A frontier speeds up long matches: the last thread whose entry
                 // is known exact (thread 0 from the start) and its exit. Every
                 // thread after it whose segment starts at or before that exit
                 // takes the exit as its entry at once (the threads it jumps
                 // over pass it through), so a match spanning many segments costs
-                // one round, not one per segment. It starts in the third round
-                // (most chunks are done after two). The rounds still end only
-                // when no entry changes, which only the sequential parse
-                // satisfies.
+                // one round, not one per segment. It starts in the third round.
+                // A thread it reaches takes the frontier exit, which in a round
+                // that changes no exit equals the exit before it, so the
+                // stopping rule is unchanged.
                 uint32_t T[4] = {0u, 0u, 0u, 0u};  // step of each position, one byte each
                 {
                     uint32_t lw[8];
@@ -791,6 +799,7 @@ __global__ void __launch_bounds__(256, 4) encode_kernel(EncodeArgs a) {
                 }
                 if (tid == 0) s_misc[24] = exit_abs;  // frontier: thread 0, its exit
                 for (uint32_t rnd = 0;; ++rnd) {
+                    const uint32_t exit_before = exit_abs;
                     uint32_t prev = __shfl_up_sync(FULL, exit_abs, 1);
                     if (lane == 31) s_misc[8 + warp] = exit_abs;
                     __syncthreads();
@@ -840,7 +849,7 @@ __global__ void __launch_bounds__(256, 4) encode_kernel(EncodeArgs a) {
                         else if (tid == 0 && fx >= E)
                             s_misc[25 - fb] = fr;
                     }
-                    if (!__syncthreads_or(changed)) break;
+                    if (!__syncthreads_or(exit_abs != exit_before)) break;
                 }
 
                 // ---- E7 (sizes): team scan of item and match counts ----

@@ -139,9 +139,12 @@ def and_chains(m, E, SEGP):
     return out
 
 
-def segment_parse(step, SEGP, frontier_from=2):
+def segment_parse(step, SEGP, frontier_from=2, stop_on_exits=True):
     """Greedy parse by per-segment walks and fixpoint rounds, with the
-    exact-entry frontier from round `frontier_from` on. Returns (path, rounds)."""
+    exact-entry frontier from round `frontier_from` on. The rounds end once a
+    round changed no segment's exit (`stop_on_exits`, the kernel's rule: every
+    entry then equals the exit before it, the fixpoint) or, the slower rule,
+    no segment's entry. Returns (path, rounds)."""
     E = len(step)
     nthr = E // SEGP
 
@@ -180,9 +183,10 @@ def segment_parse(step, SEGP, frontier_from=2):
                 fr[fb ^ 1], wrote = (t, new[t]), True
         if use and not wrote:
             fr[fb ^ 1] = fr[fb]
+        exit_changed = new != exits
         exits = new
         rnd += 1
-        if not changed:
+        if not (exit_changed if stop_on_exits else changed):
             return set().union(*paths), rnd
 
 
@@ -262,8 +266,9 @@ def test_segment_parse_equals_serial_parse():
             step[j] = min(step[j], E - j)
         ref = serial_parse(step)
         for start in (0, 2, 10 ** 9):  # frontier from the start, from round 3, never
-            got, _ = segment_parse(step, SEGP, start)
-            assert got == ref, (trial, start)
+            for stop_on_exits in (True, False):
+                got, _ = segment_parse(step, SEGP, start, stop_on_exits)
+                assert got == ref, (trial, start, stop_on_exits)
 
 
 def test_frontier_bounds_rounds_on_long_runs():
