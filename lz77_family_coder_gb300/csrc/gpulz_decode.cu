@@ -119,6 +119,15 @@ __device__ __forceinline__ void write_chunk(uint8_t* out, uint32_t take, bool ou
     }
 }
 
+// e = s_src[e] unless e is resolved (kLit set); `base` = shared address of s_src.
+__device__ __forceinline__ void follow(uint32_t& e, uint32_t base) {
+    asm volatile("{\n\t.reg .pred p;\n\t.reg .b32 t;\n\tand.b32 t, %0, 32768;\n\tsetp.eq.u32 p, t, 0;\n\t"
+                 "@p ld.shared.u16 %0, [%1];\n\t}"
+                 : "+r"(e)
+                 : "r"(base + 2u * e)
+                 : "memory");
+}
+
 template <int WS>
 __device__ uint32_t lit_word(const uint8_t* s_data, const uint16_t* s_src, uint32_t j) {
     // chunk bytes [4j, 4j + 4) = elements [4j/WS, (4j+4)/WS)
@@ -399,24 +408,25 @@ __device__ void decode_chunks(const DecodeArgs& a, const Geo& g, uint8_t* slot_b
         __syncwarp();
 
         // ---- D5: pointer jumping ----
-        // Elements in pairs: one 32-bit shared load and store per two.
-        // Entries change only towards their final value, so a concurrent
-        // reader sees an old or a new pointer, and both are valid.
+        // Elements in pairs: one 32-bit shared load and store per two; an
+        // unresolved entry follows its pointer by a predicated load and a
+        // resolved one loads nothing (no branch; measured +1-3 % decode over
+        // a select of the address, which +5-13 % beat skipping resolved pairs
+        // by a branch). Entries change only towards their final value, so a
+        // concurrent reader sees an old or a new pointer, and both are valid.
         bool unresolved = true;
         uint32_t* s_src2 = reinterpret_cast<uint32_t*>(s_src);
+        const uint32_t src_base = (uint32_t)__cvta_generic_to_shared(s_src);
         for (int r = 0; r < kMaxJumpRounds && unresolved; ++r) {
             bool mine = false;
 #pragma unroll 2
             for (uint32_t j = lane; j < E / 2u; j += 32) {
                 const uint32_t v = s_src2[j];
-                const uint32_t lo = v & 0xFFFFu, hi = v >> 16;
-                const bool rl = !(lo & kLit), rh = !(hi & kLit);
-                // a resolved entry reads its own slot (unchanged): no branch
-                // (measured: +5-13 % decode against skipping resolved pairs)
-                const uint32_t nlo = s_src[rl ? lo : 2u * j];
-                const uint32_t nhi = s_src[rh ? hi : 2u * j + 1u];
+                uint32_t nlo = v & 0xFFFFu, nhi = v >> 16;
+                follow(nlo, src_base);
+                follow(nhi, src_base);
                 s_src2[j] = nlo | (nhi << 16);
-                mine |= !(nlo & kLit) || !(nhi & kLit);
+                mine |= (nlo & nhi & kLit) == 0u;
             }
             unresolved = __any_sync(FULL, mine);
             __syncwarp();

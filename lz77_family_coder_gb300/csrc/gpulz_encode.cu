@@ -599,8 +599,9 @@ __global__ void __launch_bounds__(256, 4) encode_kernel(EncodeArgs a) {
                     for (int p = 0; p < SEGP; p += 2) {
                         const uint32_t l0 = (lb[p >> 2] >> (8 * (p & 3))) & 0xFFu;
                         const uint32_t l1 = (lb[p >> 2] >> (8 * ((p + 1) & 3))) & 0xFFu;
-                        const uint32_t lo0 = l0 ? (l0 | ((uint32_t)__ffs(cc[p]) << 8)) : 0u;
-                        const uint32_t lo1 = l1 ? (l1 | ((uint32_t)__ffs(cc[p + 1]) << 8)) : 0u;
+                        // cc[p] is 0 exactly when the length is 0 (no offset matched)
+                        const uint32_t lo0 = l0 | ((uint32_t)__ffs(cc[p]) << 8);
+                        const uint32_t lo1 = l1 | ((uint32_t)__ffs(cc[p + 1]) << 8);
                         lw[p >> 1] = lo0 | (lo1 << 16);
                     }
                     uint4* dlo = reinterpret_cast<uint4*>(s_lo + seg_a);
@@ -780,12 +781,27 @@ __global__ void __launch_bounds__(256, 4) encode_kernel(EncodeArgs a) {
                     } else {
                         lw[4] = lw[5] = lw[6] = lw[7] = 0u;
                     }
+                    if (WS != 1) {
+                        // four lengths per word (one byte permute); a byte below
+                        // LMIN (0, or 1 for word size 2) is a literal: step 1
 #pragma unroll
-                    for (int k = 0; k < SEGP; ++k) {
-                        const uint32_t len = (lw[k >> 1] >> (16 * (k & 1))) & 0xFFu;
-                        const bool mt = len >= LMIN;
-                        T[k >> 2] |= (mt ? len : 1u) << (8 * (k & 3));
-                        mmask |= (uint32_t)mt << k;
+                        for (int w = 0; w < SEGP / 4; ++w) {
+                            const uint32_t t = __byte_perm(lw[2 * w], lw[2 * w + 1], 0x6420u);
+                            const uint32_t u = WS == 2 ? (t & 0xFEFEFEFEu) : t;
+                            // 0x80 in each byte of u that is zero
+                            const uint32_t z = ~(((u & 0x7F7F7F7Fu) + 0x7F7F7F7Fu) | u | 0x7F7F7F7Fu);
+                            T[w] = t | (z >> 7);
+                            const uint32_t mt = ((~z >> 7) & 0x01010101u) * 0x01020408u >> 24;  // 4 bits
+                            mmask |= mt << (4 * w);
+                        }
+                    } else {
+#pragma unroll
+                        for (int k = 0; k < SEGP; ++k) {
+                            const uint32_t len = (lw[k >> 1] >> (16 * (k & 1))) & 0xFFu;
+                            const bool mt = len >= LMIN;
+                            T[k >> 2] |= (mt ? len : 1u) << (8 * (k & 3));
+                            mmask |= (uint32_t)mt << k;
+                        }
                     }
                 }
                 uint32_t cur_e = 0, exit_abs;
