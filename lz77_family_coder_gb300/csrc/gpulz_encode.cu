@@ -174,6 +174,13 @@ __device__ __forceinline__ void or_if_equal(uint32_t& mm, uint32_t a, uint32_t b
         : "r"(a), "r"(b), "r"(bit));
 }
 
+// an |= bit where x != 0: one test and one predicated OR.
+__device__ __forceinline__ void or_if_nonzero(uint32_t& an, uint32_t x, uint32_t bit) {
+    asm("{\n\t.reg .pred q;\n\tsetp.ne.u32 q, %1, 0;\n\t@q or.b32 %0, %0, %2;\n\t}"
+        : "+r"(an)
+        : "r"(x), "r"(bit));
+}
+
 // One AND-chain step of chain p (bit = 1 << p): x = c & m; where bit p of
 // `live` is set and x != 0, c = x and bit p of `an` is set.
 __device__ __forceinline__ void chain_step(uint32_t& c, uint32_t& an, uint32_t m, uint32_t live, uint32_t bit) {
@@ -312,7 +319,7 @@ __device__ __forceinline__ void and_chains(const uint32_t (&m)[SEGP], const uint
 #pragma unroll
     for (int p = 0; p < SEGP; ++p) {
         cc[p] = m[p];
-        A |= (uint32_t)(m[p] != 0u) << p;
+        or_if_nonzero(A, m[p], 1u << p);
     }
     uint32_t lb[SEGP / 4];
 #pragma unroll
@@ -466,8 +473,8 @@ __global__ void __launch_bounds__(256, 4) encode_kernel(EncodeArgs a) {
                 const uint4* src = reinterpret_cast<const uint4*>(a.in + begin);
                 for (uint32_t g = tid; g < CS / 16u; g += nthreads) {
                     const uint4 v = __ldg(src + g);
-                    uint32_t* dst = reinterpret_cast<uint32_t*>(s_el + chunk_byte_addr<WS>(16u * g));
-                    dst[0] = v.x; dst[1] = v.y; dst[2] = v.z; dst[3] = v.w;
+                    // 16 chunk bytes stay 16-byte aligned in the padded array
+                    *reinterpret_cast<uint4*>(s_el + chunk_byte_addr<WS>(16u * g)) = v;
                     if (LEVEL && !SINGLE) reinterpret_cast<uint4*>(s_data)[g] = v;
                     nz |= v.x | v.y | v.z | v.w;
                 }
@@ -518,7 +525,7 @@ __global__ void __launch_bounds__(256, 4) encode_kernel(EncodeArgs a) {
 #pragma unroll
                     for (int p = 0; p < SEGP; ++p) {
                         cc[p] = m[p];
-                        A |= (uint32_t)(m[p] != 0u) << p;
+                        or_if_nonzero(A, m[p], 1u << p);
                     }
                     uint32_t lb[SEGP / 4];
 #pragma unroll
