@@ -616,7 +616,7 @@ __global__ void __launch_bounds__(256, 4) encode_kernel(EncodeArgs a) {
                     for (int q = 0; q < SEGP / 8; ++q)
                         dlo[q] = make_uint4(lw[4 * q], lw[4 * q + 1], lw[4 * q + 2], lw[4 * q + 3]);
                 }
-                __syncthreads();
+                if constexpr (NEARW > 32) __syncthreads();  // the far pass reuses the masks' area
 
                 // ---- E4b (near windows wider than 32): offsets 33..window ----
                 // A second set of masks over the same positions replaces the
