@@ -233,9 +233,14 @@ __device__ __forceinline__ void near_masks(const uint8_t* s_el, uint32_t base, u
             uint32_t mm = 0;
 #pragma unroll
             for (int o = 1; o <= 32; ++o) or_if_equal(mm, v[32 + p - o], x, 1u << (o - 1));
-            const uint32_t i = base + (uint32_t)(8 * h + p);
-            if (i < 32u) mm &= (1u << i) - 1u;
             m[8 * h + p] = mm;
+        }
+    }
+    if (base < 32u) {  // positions whose window starts before the chunk (the first threads only)
+#pragma unroll
+        for (int p = 0; p < SEGP; ++p) {
+            const uint32_t i = base + (uint32_t)p;
+            if (i < 32u) m[p] &= (1u << i) - 1u;
         }
     }
 }
