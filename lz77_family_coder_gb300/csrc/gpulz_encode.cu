@@ -677,11 +677,14 @@ __global__ void __launch_bounds__(256, 4) encode_kernel(EncodeArgs a) {
                     uint32_t cm = 0;      // owned positions with a candidate
 #pragma unroll
                     for (int s = 0; s < kSubBlocks; ++s) {
+                        // only the chunk's last position (the last sub-block's last
+                        // owned position of the last thread) has no two-word key
                         uint32_t hk[R];
 #pragma unroll
                         for (int r = 0; r < R; ++r) {
                             const uint32_t i = (uint32_t)s * SB + (uint32_t)r * (uint32_t)nthreads + (uint32_t)tid;
-                            const uint32_t i1 = i + 1u < E ? i + 1u : i;
+                            const bool key = (s + 1 < kSubBlocks || r + 1 < R) || (uint32_t)tid + 1u < (uint32_t)nthreads;
+                            const uint32_t i1 = key ? i + 1u : i;
                             hk[r] = SINGLE ? key_hash(el_get<WS>(s_el, i), el_get<WS>(s_el, i1), a.hash_bits)
                                            : key_hash(lin_get<WS>(s_data, i), lin_get<WS>(s_data, i1), a.hash_bits);
                         }
@@ -690,11 +693,12 @@ __global__ void __launch_bounds__(256, 4) encode_kernel(EncodeArgs a) {
                             for (int r = 0; r < R; ++r) {
                                 const int j = s * R + r;
                                 const uint32_t i = (uint32_t)s * SB + (uint32_t)r * (uint32_t)nthreads + (uint32_t)tid;
+                                const bool key = (s + 1 < kSubBlocks || r + 1 < R) || (uint32_t)tid + 1u < (uint32_t)nthreads;
                                 const uint32_t slot = s_tab[hk[r]];
                                 const uint32_t d = i + 1u - (slot & 0xFFFFu);  // i - p for p = slot - 1
                                 // this chunk's entry (tag), 32 < d <= kMaxOff, a key at i
                                 const bool ok = ((slot ^ (tag << 16)) < 0x10000u) &
-                                                (d - 33u < (uint32_t)(kMaxOff - 32)) & (i + 1u < E);
+                                                (d - 33u < (uint32_t)(kMaxOff - 32)) & key;
                                 if (ok) {
                                     cd[j >> 2] |= d << (8 * (j & 3));
                                     cm |= 1u << j;
@@ -706,7 +710,7 @@ __global__ void __launch_bounds__(256, 4) encode_kernel(EncodeArgs a) {
 #pragma unroll
                             for (int r = 0; r < R; ++r) {
                                 const uint32_t i = (uint32_t)s * SB + (uint32_t)r * (uint32_t)nthreads + (uint32_t)tid;
-                                if (i + 1u < E) atomicMax(&s_tab[hk[r]], (tag << 16) | (i + 1u));
+                                atomicMax(&s_tab[hk[r]], (tag << 16) | (i + 1u));  // s < 7: every position has a key
                             }
                             __syncthreads();  // inserts before the next sub-block's lookups
                         }
