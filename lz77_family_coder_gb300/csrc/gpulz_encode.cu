@@ -209,9 +209,12 @@ __device__ __forceinline__ void near_masks(const uint8_t* s_el, uint32_t base, u
         uint32_t v[40];
 #pragma unroll
         for (int q = 0; q < 10; ++q) {
-            const int i0 = first + 4 * q;
-            uint32_t w[4] = {0u, 0u, 0u, 0u};
-            if (i0 >= 0) {
+            // a window element before the chunk is read from element 0 instead:
+            // it only meets offsets past the position, whose bits the head
+            // masking below clears
+            const int i0 = max(first + 4 * q, 0);
+            uint32_t w[4];
+            {
                 const uint8_t* p = s_el + el_addr<WS>((uint32_t)i0);
                 if (WS == 4) {
                     const uint4 t = *reinterpret_cast<const uint4*>(p);
