@@ -160,12 +160,13 @@ __device__ void write_header_split(const EncodeArgs& a, uint32_t ws, uint64_t me
         atomicOr(a.status, kStatCapacity);
 }
 
-// The two steps below are written as predicated PTX because the plain C forms
+// The steps below are written as predicated PTX because the plain C forms
 // (`mm |= (a == b) ? bit : 0`, and a select of the chain's new mask) compile
 // to a compare, a select and an OR on the integer pipe, which bounds this
 // kernel; the near masks alone are 32 compares per element. Measured, all
 // streams unchanged: near masks +8-18 % encode on every workload, chain steps
-// and verification compares a further +3-10 %.
+// and verification compares a further +3-10 %, and chains that hold 0 once
+// dead (no liveness test per step) +3-10 % more.
 //
 // mm |= bit where a == b: one compare and one predicated OR.
 __device__ __forceinline__ void or_if_equal(uint32_t& mm, uint32_t a, uint32_t b, uint32_t bit) {
@@ -174,25 +175,20 @@ __device__ __forceinline__ void or_if_equal(uint32_t& mm, uint32_t a, uint32_t b
         : "r"(a), "r"(b), "r"(bit));
 }
 
+// One AND-chain step for chains that hold 0 once dead: c &= m; where the
+// result is nonzero, keep = c and an |= bit.
+__device__ __forceinline__ void chain_step(uint32_t& c, uint32_t& keep, uint32_t& an, uint32_t m, uint32_t bit) {
+    asm("{\n\t.reg .pred q;\n\tand.b32 %0, %0, %3;\n\tsetp.ne.u32 q, %0, 0;\n\t"
+        "@q mov.b32 %1, %0;\n\t@q or.b32 %2, %2, %4;\n\t}"
+        : "+r"(c), "+r"(keep), "+r"(an)
+        : "r"(m), "r"(bit));
+}
+
 // an |= bit where x != 0: one test and one predicated OR.
 __device__ __forceinline__ void or_if_nonzero(uint32_t& an, uint32_t x, uint32_t bit) {
     asm("{\n\t.reg .pred q;\n\tsetp.ne.u32 q, %1, 0;\n\t@q or.b32 %0, %0, %2;\n\t}"
         : "+r"(an)
         : "r"(x), "r"(bit));
-}
-
-// One AND-chain step of chain p (bit = 1 << p): x = c & m; where bit p of
-// `live` is set and x != 0, c = x and bit p of `an` is set.
-__device__ __forceinline__ void chain_step(uint32_t& c, uint32_t& an, uint32_t m, uint32_t live, uint32_t bit) {
-    asm("{\n\t.reg .pred q, r;\n\t.reg .b32 x, y;\n\t"
-        "and.b32 x, %0, %2;\n\t"
-        "and.b32 y, %3, %4;\n\t"
-        "setp.ne.u32 r, y, 0;\n\t"
-        "setp.ne.and.u32 q, x, 0, r;\n\t"
-        "@q mov.b32 %0, x;\n\t"
-        "@q or.b32 %1, %1, %4;\n\t}"
-        : "+r"(c), "+r"(an)
-        : "r"(m), "r"(live), "r"(bit));
 }
 
 // ---------------------------------------------------------------------------
@@ -322,11 +318,12 @@ template <int SEGP>
 __device__ __forceinline__ void and_chains(const uint32_t (&m)[SEGP], const uint32_t* s_om,
                                            const uint32_t* s_sa, uint32_t seg_a, uint32_t E,
                                            uint32_t off_base, uint32_t (&lw)[SEGP / 2]) {
-    uint32_t cc[SEGP];
+    uint32_t cc[SEGP], cl[SEGP];  // running AND (0 once dead), last nonzero value
     uint32_t A = 0;
 #pragma unroll
     for (int p = 0; p < SEGP; ++p) {
         cc[p] = m[p];
+        cl[p] = m[p];
         or_if_nonzero(A, m[p], 1u << p);
     }
     uint32_t lb[SEGP / 4];
@@ -340,7 +337,7 @@ __device__ __forceinline__ void and_chains(const uint32_t (&m)[SEGP], const uint
         uint32_t An = 0;
 #pragma unroll
         for (int p = 0; p + k < SEGP; ++p) {
-            chain_step(cc[p], An, m[p + k], act, 1u << p);
+            chain_step(cc[p], cl[p], An, m[p + k], 1u << p);
         }
 #pragma unroll
         for (int w = 0; w < SEGP / 4; ++w) lb[w] += expand4((An >> (4 * w)) & 15u);
@@ -367,8 +364,10 @@ __device__ __forceinline__ void and_chains(const uint32_t (&m)[SEGP], const uint
                 }
                 if (take) {
 #pragma unroll
-                    for (int p = 0; p < SEGP; ++p)
-                        if ((A2 >> p) & 1u) cc[p] &= sa;
+                    for (int p = 0; p < SEGP; ++p) {
+                        cc[p] &= sa;  // dead chains stay 0
+                        if ((A2 >> p) & 1u) cl[p] = cc[p];
+                    }
 #pragma unroll
                     for (int w = 0; w < SEGP / 4; ++w) lb[w] += take * expand4((A2 >> (4 * w)) & 15u);
                     st += take;
@@ -380,12 +379,18 @@ __device__ __forceinline__ void and_chains(const uint32_t (&m)[SEGP], const uint
                 uint32_t An = 0;
 #pragma unroll
                 for (int p = 0; p < SEGP; ++p) {
-                    chain_step(cc[p], An, om, A2, 1u << p);
+                    chain_step(cc[p], cl[p], An, om, 1u << p);
                 }
 #pragma unroll
                 for (int w = 0; w < SEGP / 4; ++w) lb[w] += expand4((An >> (4 * w)) & 15u);
                 const int over = (int)(SEGP + st + 1u) - kMaxLen;
-                if (over >= 0) An &= ~((2u << (over < SEGP - 1 ? over : SEGP - 1)) - 1u);
+                if (over >= 0) {
+                    const int lim = over < SEGP - 1 ? over : SEGP - 1;
+                    An &= ~((2u << lim) - 1u);
+#pragma unroll
+                    for (int p = 0; p < SEGP; ++p)
+                        if (p <= lim) cc[p] = 0;  // capped chains end here
+                }
                 A2 = An;
             }
         }
@@ -394,8 +399,8 @@ __device__ __forceinline__ void and_chains(const uint32_t (&m)[SEGP], const uint
     for (int p = 0; p < SEGP; p += 2) {
         const uint32_t l0 = (lb[p >> 2] >> (8 * (p & 3))) & 0xFFu;
         const uint32_t l1 = (lb[p >> 2] >> (8 * ((p + 1) & 3))) & 0xFFu;
-        const uint32_t lo0 = l0 ? (l0 | ((off_base + (uint32_t)__ffs(cc[p])) << 8)) : 0u;
-        const uint32_t lo1 = l1 ? (l1 | ((off_base + (uint32_t)__ffs(cc[p + 1])) << 8)) : 0u;
+        const uint32_t lo0 = l0 ? (l0 | ((off_base + (uint32_t)__ffs(cl[p])) << 8)) : 0u;
+        const uint32_t lo1 = l1 ? (l1 | ((off_base + (uint32_t)__ffs(cl[p + 1])) << 8)) : 0u;
         lw[p >> 1] = lo0 | (lo1 << 16);
     }
 }
@@ -528,11 +533,14 @@ __global__ void __launch_bounds__(256, 4) encode_kernel(EncodeArgs a) {
                 // registers; one that is still alive at the segment end is
                 // finished from the shared-memory masks.
                 {
-                    uint32_t cc[SEGP];
+                    // cc[p]: chain p's running AND, 0 once it died; cl[p]: its
+                    // last nonzero value (the nearest offset is its lowest bit)
+                    uint32_t cc[SEGP], cl[SEGP];
                     uint32_t A = 0;
 #pragma unroll
                     for (int p = 0; p < SEGP; ++p) {
                         cc[p] = m[p];
+                        cl[p] = m[p];
                         or_if_nonzero(A, m[p], 1u << p);
                     }
                     uint32_t lb[SEGP / 4];
@@ -546,7 +554,7 @@ __global__ void __launch_bounds__(256, 4) encode_kernel(EncodeArgs a) {
                         uint32_t An = 0;
 #pragma unroll
                         for (int p = 0; p + k < SEGP; ++p) {
-                            chain_step(cc[p], An, m[p + k], act, 1u << p);
+                            chain_step(cc[p], cl[p], An, m[p + k], 1u << p);
                         }
 #pragma unroll
                         for (int w = 0; w < SEGP / 4; ++w) lb[w] += expand4((An >> (4 * w)) & 15u);
@@ -584,8 +592,10 @@ __global__ void __launch_bounds__(256, 4) encode_kernel(EncodeArgs a) {
                                 }
                                 if (take) {
 #pragma unroll
-                                    for (int p = 0; p < SEGP; ++p)
-                                        if ((A2 >> p) & 1u) cc[p] &= sa;
+                                    for (int p = 0; p < SEGP; ++p) {
+                                        cc[p] &= sa;  // dead chains stay 0
+                                        if ((A2 >> p) & 1u) cl[p] = cc[p];
+                                    }
 #pragma unroll
                                     for (int w = 0; w < SEGP / 4; ++w)
                                         lb[w] += take * expand4((A2 >> (4 * w)) & 15u);
@@ -597,14 +607,18 @@ __global__ void __launch_bounds__(256, 4) encode_kernel(EncodeArgs a) {
                                 const uint32_t om = s_om[om_idx(q0 + (uint32_t)k)];
                                 uint32_t An = 0;
 #pragma unroll
-                                for (int p = 0; p < SEGP; ++p) {
-                                    chain_step(cc[p], An, om, A2, 1u << p);
-                                }
+                                for (int p = 0; p < SEGP; ++p) chain_step(cc[p], cl[p], An, om, 1u << p);
 #pragma unroll
                                 for (int w = 0; w < SEGP / 4; ++w) lb[w] += expand4((An >> (4 * w)) & 15u);
                                 // length of chain p is now SEGP - p + st + 1: stop at the cap
                                 const int over = (int)(SEGP + st + 1u) - kMaxLen;
-                                if (over >= 0) An &= ~((2u << (over < SEGP - 1 ? over : SEGP - 1)) - 1u);
+                                if (over >= 0) {
+                                    const int lim = over < SEGP - 1 ? over : SEGP - 1;
+                                    An &= ~((2u << lim) - 1u);
+#pragma unroll
+                                    for (int p = 0; p < SEGP; ++p)
+                                        if (p <= lim) cc[p] = 0;  // capped chains end here
+                                }
                                 A2 = An;
                             }
                         }
@@ -614,9 +628,9 @@ __global__ void __launch_bounds__(256, 4) encode_kernel(EncodeArgs a) {
                     for (int p = 0; p < SEGP; p += 2) {
                         const uint32_t l0 = (lb[p >> 2] >> (8 * (p & 3))) & 0xFFu;
                         const uint32_t l1 = (lb[p >> 2] >> (8 * ((p + 1) & 3))) & 0xFFu;
-                        // cc[p] is 0 exactly when the length is 0 (no offset matched)
-                        const uint32_t lo0 = l0 | ((uint32_t)__ffs(cc[p]) << 8);
-                        const uint32_t lo1 = l1 | ((uint32_t)__ffs(cc[p + 1]) << 8);
+                        // cl[p] is 0 exactly when the length is 0 (no offset matched)
+                        const uint32_t lo0 = l0 | ((uint32_t)__ffs(cl[p]) << 8);
+                        const uint32_t lo1 = l1 | ((uint32_t)__ffs(cl[p + 1]) << 8);
                         lw[p >> 1] = lo0 | (lo1 << 16);
                     }
                     uint4* dlo = reinterpret_cast<uint4*>(s_lo + seg_a);
