@@ -374,8 +374,9 @@ __device__ __forceinline__ void and_chains(const uint32_t (&m)[SEGP], const uint
                     continue;
                 }
             }
+            const uint32_t* omq = s_om + om_idx(q0);  // one 16-mask block
             for (int k = 0; k < SEGP && A2 != 0u; ++k, ++st) {
-                const uint32_t om = s_om[om_idx(q0 + (uint32_t)k)];
+                const uint32_t om = omq[k];
                 uint32_t An = 0;
 #pragma unroll
                 for (int p = 0; p < SEGP; ++p) {
@@ -603,8 +604,10 @@ __global__ void __launch_bounds__(256, 4) encode_kernel(EncodeArgs a) {
                                     continue;
                                 }
                             }
+                            // the segment's masks are contiguous (one 16-mask block)
+                            const uint32_t* omq = s_om + om_idx(q0);
                             for (int k = 0; k < SEGP && A2 != 0u; ++k, ++st) {
-                                const uint32_t om = s_om[om_idx(q0 + (uint32_t)k)];
+                                const uint32_t om = omq[k];
                                 uint32_t An = 0;
 #pragma unroll
                                 for (int p = 0; p < SEGP; ++p) chain_step(cc[p], cl[p], An, om, 1u << p);
