@@ -210,18 +210,16 @@ __device__ __forceinline__ void near_masks(const uint8_t* s_el, uint32_t base, u
             // masking below clears
             const int i0 = max(first + 4 * q, 0);
             uint32_t w[4];
-            {
-                const uint8_t* p = s_el + el_addr<WS>((uint32_t)i0);
-                if (WS == 4) {
-                    const uint4 t = *reinterpret_cast<const uint4*>(p);
-                    w[0] = t.x; w[1] = t.y; w[2] = t.z; w[3] = t.w;
-                } else if (WS == 2) {
-                    const uint2 t = *reinterpret_cast<const uint2*>(p);
-                    w[0] = t.x & 0xFFFFu; w[1] = t.x >> 16; w[2] = t.y & 0xFFFFu; w[3] = t.y >> 16;
-                } else {
-                    const uint32_t t = *reinterpret_cast<const uint32_t*>(p);
-                    w[0] = t & 0xFFu; w[1] = (t >> 8) & 0xFFu; w[2] = (t >> 16) & 0xFFu; w[3] = t >> 24;
-                }
+            const uint8_t* p = s_el + el_addr<WS>((uint32_t)i0);
+            if (WS == 4) {
+                const uint4 t = *reinterpret_cast<const uint4*>(p);
+                w[0] = t.x; w[1] = t.y; w[2] = t.z; w[3] = t.w;
+            } else if (WS == 2) {
+                const uint2 t = *reinterpret_cast<const uint2*>(p);
+                w[0] = t.x & 0xFFFFu; w[1] = t.x >> 16; w[2] = t.y & 0xFFFFu; w[3] = t.y >> 16;
+            } else {
+                const uint32_t t = *reinterpret_cast<const uint32_t*>(p);
+                w[0] = t & 0xFFu; w[1] = (t >> 8) & 0xFFu; w[2] = (t >> 16) & 0xFFu; w[3] = t >> 24;
             }
 #pragma unroll
             for (int r = 0; r < 4; ++r) v[4 * q + r] = w[r];
