@@ -419,7 +419,7 @@ __device__ void decode_chunks(const DecodeArgs& a, const Geo& g, uint8_t* slot_b
         const uint32_t src_base = (uint32_t)__cvta_generic_to_shared(s_src);
         for (int r = 0; r < kMaxJumpRounds && unresolved; ++r) {
             bool mine = false;
-#pragma unroll 2
+#pragma unroll 4
             for (uint32_t j = lane; j < E / 2u; j += 32) {
                 const uint32_t v = s_src2[j];
                 uint32_t nlo = v & 0xFFFFu, nhi = v >> 16;
