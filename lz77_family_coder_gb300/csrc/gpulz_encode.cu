@@ -191,6 +191,13 @@ __device__ __forceinline__ void or_if_nonzero(uint32_t& an, uint32_t x, uint32_t
         : "r"(x), "r"(bit));
 }
 
+// Shared-memory byte store under a predicate (the byte staging pass).
+__device__ __forceinline__ void st8_if(uint32_t on, uint8_t* p, uint32_t v) {
+    asm volatile("{\n\t.reg .pred q;\n\tsetp.ne.u32 q, %0, 0;\n\t@q st.shared.u8 [%1], %2;\n\t}"
+                 ::"r"(on), "r"((uint32_t)__cvta_generic_to_shared(p)), "h"((uint16_t)(v & 0xFFu))
+                 : "memory");
+}
+
 // ---------------------------------------------------------------------------
 // Per-segment near masks (E3): m[p] bit o-1 set iff element (base+p) equals
 // element (base+p-o), 1 <= o <= 32, base+p-o >= 0.
@@ -1042,23 +1049,33 @@ __global__ void __launch_bounds__(256, 4) encode_kernel(EncodeArgs a) {
                         }
                     }
                     uint32_t fbits = 0, k = 0;
+                    if (WS == 1) {
+                        // bytes: predicated stores and arithmetic offsets, no
+                        // branch per position (+3 % on the byte stream; the
+                        // wider words keep the branches, measured 0.4 % faster)
 #pragma unroll
-                    for (int p = 0; p < SEGP; ++p) {
+                        for (int p = 0; p < SEGP; ++p) {
+                            const uint32_t on = (path >> p) & 1u;
+                            const uint32_t ism = (mmask >> p) & 1u;
+                            const uint32_t tok = (lo[p >> 1] >> (16 * (p & 1))) & 0xFFFFu;
+                            const uint32_t e = (ew[p >> 2] >> (8 * (p & 3))) & 0xFFu;
+                            st8_if(on, s_data + bb, ism ? tok : e);
+                            st8_if(on & ism, s_data + bb + 1, tok >> 8);
+                            bb += on * (1u + ism);
+                            fbits |= (on & ism) << k;
+                            k += on;
+                        }
+                    }
+#pragma unroll
+                    for (int p = 0; p < SEGP && WS != 1; ++p) {
                         if (!((path >> p) & 1u)) continue;
                         if ((mmask >> p) & 1u) {
                             const uint32_t v = (lo[p >> 1] >> (16 * (p & 1))) & 0xFFFFu;
-                            if (WS == 1) {
-                                s_data[bb] = (uint8_t)v;
-                                s_data[bb + 1] = (uint8_t)(v >> 8);
-                            } else {
-                                *reinterpret_cast<uint16_t*>(s_data + bb) = (uint16_t)v;
-                            }
+                            *reinterpret_cast<uint16_t*>(s_data + bb) = (uint16_t)v;
                             bb += 2u;
                             fbits |= 1u << k;
                         } else {
-                            if (WS == 1) {
-                                s_data[bb] = (uint8_t)(ew[p >> 2] >> (8 * (p & 3)));
-                            } else if (WS == 2) {
+                            if (WS == 2) {
                                 *reinterpret_cast<uint16_t*>(s_data + bb) = (uint16_t)(ew[p >> 1] >> (16 * (p & 1)));
                             } else {
                                 *reinterpret_cast<uint16_t*>(s_data + bb) = (uint16_t)ew[p];
