@@ -836,12 +836,17 @@ __global__ void __launch_bounds__(256, 4) encode_kernel(EncodeArgs a) {
                             mmask |= mt << (4 * w);
                         }
                     } else {
+                        // bytes (LMIN 3): 0x80 where a length is >= 3 (bit 7 of
+                        // (len | 0x80) - 3, or of len itself), then step = len
+                        // there and 1 elsewhere
+                        static_assert(WS != 1 || LMIN == 3u, "byte lengths below 3 are literals");
 #pragma unroll
-                        for (int k = 0; k < SEGP; ++k) {
-                            const uint32_t len = (lw[k >> 1] >> (16 * (k & 1))) & 0xFFu;
-                            const bool mt = len >= LMIN;
-                            T[k >> 2] |= (mt ? len : 1u) << (8 * (k & 3));
-                            mmask |= (uint32_t)mt << k;
+                        for (int w = 0; w < SEGP / 4; ++w) {
+                            const uint32_t t = __byte_perm(lw[2 * w], lw[2 * w + 1], 0x6420u);
+                            const uint32_t f = (((t | 0x80808080u) - 0x03030303u) | t) & 0x80808080u;
+                            const uint32_t keep = (f >> 7) * 0xFFu;
+                            T[w] = (t & keep) | (~keep & 0x01010101u);
+                            mmask |= ((((f >> 7) & 0x01010101u) * 0x01020408u) >> 24) << (4 * w);
                         }
                     }
                 }
