@@ -190,6 +190,90 @@ def segment_parse(step, SEGP, frontier_from=2, stop_on_exits=True):
             return set().union(*paths), rnd
 
 
+def and_chains_zeroed(m, E, SEGP):
+    """The same chains in the representation the kernel steps them in: a
+    chain's running AND is left at 0 once it dies (so a step needs no liveness
+    test: AND, and where the result is nonzero keep it and set the survivor
+    bit), the last nonzero value is kept aside for the offset, the lengths are
+    counted from the survivor bits, and a chain reaching the cap is zeroed."""
+    sa = []
+    for t in range(E // SEGP):
+        a = 0xFFFFFFFF
+        for p in range(SEGP):
+            a &= m[t * SEGP + p]
+        sa.append(a)
+    out = []
+    for t in range(E // SEGP):
+        seg_a = t * SEGP
+        cc = [m[seg_a + p] for p in range(SEGP)]
+        keep = cc[:]
+        A = sum(1 << p for p in range(SEGP) if cc[p])
+        L = [(A >> p) & 1 for p in range(SEGP)]
+        P = A & (1 << (SEGP - 1))
+        for k in range(1, SEGP):
+            act = A & ((1 << (SEGP - k)) - 1)
+            if not act:
+                break
+            An = 0
+            for p in range(SEGP - k):  # no liveness test: dead chains hold 0
+                cc[p] &= m[seg_a + p + k]
+                if cc[p]:
+                    keep[p] = cc[p]
+                    An |= 1 << p
+            for p in range(SEGP):
+                L[p] += (An >> p) & 1
+            P |= An & (1 << (SEGP - 1 - k))
+            A = An
+        A2, st = P, 0
+        while A2 and seg_a + SEGP + st < E:
+            q0 = seg_a + SEGP + st
+            if A2 == (1 << SEGP) - 1 or st >= SEGP:
+                j = q0 // SEGP
+                p0 = (A2 & -A2).bit_length() - 1
+                room = MAXLEN - (SEGP - p0 + st)
+                take, s = 0, 0
+                live = [(A2 >> p) & 1 for p in range(SEGP)]
+                if room > 4 * SEGP and q0 + 4 * SEGP <= E:
+                    s = sa[j] & sa[j + 1] & sa[j + 2] & sa[j + 3]
+                    if all(not live[p] or cc[p] & s for p in range(SEGP)):
+                        take = 4 * SEGP
+                if not take and room > SEGP:
+                    s = sa[j]
+                    if all(not live[p] or cc[p] & s for p in range(SEGP)):
+                        take = SEGP
+                if take:
+                    for p in range(SEGP):
+                        cc[p] &= s  # dead chains stay 0
+                        if live[p]:
+                            keep[p] = cc[p]
+                            L[p] += take
+                    st += take
+                    continue
+            for k in range(SEGP):
+                if not A2:
+                    break
+                om = m[q0 + k]
+                An = 0
+                for p in range(SEGP):
+                    cc[p] &= om
+                    if cc[p]:
+                        keep[p] = cc[p]
+                        An |= 1 << p
+                for p in range(SEGP):
+                    L[p] += (An >> p) & 1
+                over = SEGP + st + 1 - MAXLEN
+                if over >= 0:
+                    lim = min(over, SEGP - 1)
+                    An &= ~((2 << lim) - 1)
+                    for p in range(lim + 1):
+                        cc[p] = 0
+                A2 = An
+                st += 1
+        for p in range(SEGP):
+            out.append((L[p], (keep[p] & -keep[p]).bit_length()))
+    return out
+
+
 # ----------------------------------------------------------------------------
 # inputs
 # ----------------------------------------------------------------------------
@@ -237,6 +321,16 @@ def _chunks(seed, E):
 def test_and_chains_with_skips_equal_longest_match(E, SEGP):
     for name, v in _chunks(E + SEGP, E):
         got = and_chains(masks(v), E, SEGP)
+        L, O = longest_matches(v, 32)
+        assert got == list(zip(L.tolist(), O.tolist())), name
+
+
+@pytest.mark.parametrize("E,SEGP", [(256, 8), (512, 8), (1024, 16)])
+def test_zeroed_chains_equal_longest_match(E, SEGP):
+    # the kernel's representation of the chains gives the same lengths and
+    # nearest offsets as brute force
+    for name, v in _chunks(E + 3 * SEGP, E):
+        got = and_chains_zeroed(masks(v), E, SEGP)
         L, O = longest_matches(v, 32)
         assert got == list(zip(L.tolist(), O.tolist())), name
 
