@@ -377,3 +377,30 @@ def test_frontier_bounds_rounds_on_long_runs():
     path, fast = segment_parse(step, SEGP, 2)
     assert path == serial_parse(step)
     assert plain > 30 and fast <= 10
+
+
+def test_step_byte_tricks():
+    # the parse's step bytes, built four at a time from the run-length bytes:
+    # step = len where len >= Lmin (a match), else 1 (a literal); the match
+    # bits gathered by one multiply. Lmin is 1, 2, 3 for word sizes 4, 2, 1.
+    rng = np.random.default_rng(5)
+    lens = np.concatenate([rng.integers(0, 256, (20000, 4)),
+                           rng.choice([0, 1, 2, 3, 4, 127, 128, 129, 130, 131, 255], (20000, 4))])
+    M = 0xFFFFFFFF
+    for row in lens.tolist():
+        t = row[0] | row[1] << 8 | row[2] << 16 | row[3] << 24
+        for ws, lmin in ((4, 1), (2, 2)):
+            u = t & 0xFEFEFEFE if ws == 2 else t
+            z = ~(((u & 0x7F7F7F7F) + 0x7F7F7F7F) | u | 0x7F7F7F7F) & M
+            T = t | (z >> 7)
+            mt = ((((~z & M) >> 7) & 0x01010101) * 0x01020408 & M) >> 24
+            for k in range(4):
+                assert (T >> 8 * k) & 0xFF == (row[k] if row[k] >= lmin else 1)
+                assert (mt >> k) & 1 == (row[k] >= lmin)
+        f = ((((t | 0x80808080) - 0x03030303) & M) | t) & 0x80808080
+        keep = (f >> 7) * 0xFF & M
+        T = (t & keep) | (~keep & 0x01010101 & M)
+        mt = ((((f >> 7) & 0x01010101) * 0x01020408) & M) >> 24
+        for k in range(4):
+            assert (T >> 8 * k) & 0xFF == (row[k] if row[k] >= 3 else 1)
+            assert (mt >> k) & 1 == (row[k] >= 3)
